@@ -1,0 +1,234 @@
+/*
+ * gemm_rs.h: C ABI of the fused GEMM + reduce-scatter (GEMM+RS) library
+ * for GB300 (sm_103a).
+ *
+ * OPERATION
+ *   Y_c = sum over r = 0 .. W-1 of (alpha * A_r * B_r + beta * C)[rows of chunk c]
+ *
+ *   This is the second GEMM of a tensor-parallel FFN, whose epilogue writes
+ *   into the reduce-scatter buffers instead of a plain output
+ *   ("flux实现：sm80 gemm+rs", opening paragraph; "flux精读" §3 Design).
+ *   - The W logical ranks each hold one K-shard: A_r = A[r] is [M][K/W] and
+ *     B_r = B[r] is [K/W][N].  All W shards live in one GPU's memory.
+ *   - The output Y is [M][N], made of W chunks of R = M/W contiguous rows.
+ *     Rank c keeps chunk c, and the other W-1 chunks go to the other ranks
+ *     ("flux实现：sm80 gemm+rs", section "gemmrs版本的swizzle如何编排").
+ *   - Each rank's epilogue forms alpha*acc + beta*C ("flux实现：sm80 gemm+rs",
+ *     section "custom_evt_d()": EVT_Compute0 = alpha*acc, EVT_Compute1 =
+ *     beta*C + EVT_Compute0).  So beta*C is added once per rank: the result
+ *     is alpha * sum_r(A_r B_r) + W * beta * C.  C is never read when
+ *     beta == 0.
+ *   - The partials are fp32.  They are summed in fixed rank order
+ *     ((p_0 + p_1) + p_2) + ... in fp32, so results are bit-identical from
+ *     run to run.  A bf16 Y is rounded to nearest even.
+ *
+ *   One call runs one fused kernel.  Each output tile's partial goes into a
+ *   workspace slot keyed to its chunk.  A 32-bit arrival counter per output
+ *   tile finds the last rank to arrive ("flux实现：sm80 gemm+rs", section
+ *   "evt_store_d()": a globally unique id per tile and a barrier flag per
+ *   tile; "flux精读" §4.2: signals are 32-bit contiguous memory that lives as
+ *   long as the op).  That rank's CTA reduces the tile and resets the counter
+ *   to zero.  So no memset, separate reduce kernel or host sync runs between
+ *   calls (the page's reduce buffer had to start zeroed and its clear cost tens
+ *   of microseconds: "flux实现：sm80 gemm+rs", section "自己的类flux实现").
+ *
+ * CONVENTIONS
+ *   - Every function returns GEMM_RS_OK (0) or a negative GEMM_RS_ERR_* code.
+ *     gemm_rs_last_error() then gives a message (per calling thread).  No C++
+ *     exception crosses this boundary.
+ *   - Pointers marked "device" are CUDA device addresses.  Pointers marked
+ *     "host" are ordinary host memory.
+ *   - The caller owns all device memory: A, B, C, Y and the workspace.  The
+ *     library never allocates device memory.
+ *   - A handle owns host state only (shape, TMA descriptors, launch plan).
+ *   - gemm_rs_stream_t is a cudaStream_t.  NULL means the legacy default
+ *     stream.  The calls that run on a stream are asynchronous, except
+ *     gemm_rs_status, which synchronises the stream.
+ *   - A handle's workspace holds the tile counters.  Two runs of one handle
+ *     must not overlap in time: use one stream per handle, or order the
+ *     streams.
+ */
+#ifndef GEMM_RS_H
+#define GEMM_RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(GEMM_RS_BUILD) && defined(__GNUC__)
+#define GEMM_RS_API __attribute__((visibility("default")))
+#else
+#define GEMM_RS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_rs_s *gemm_rs_t;
+typedef struct CUstream_st *gemm_rs_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    GEMM_RS_BF16 = 0,
+    GEMM_RS_FP32 = 1
+} gemm_rs_dtype;
+
+enum {
+    GEMM_RS_OK = 0,
+    GEMM_RS_ERR_ARG = -1,         /* NULL handle or pointer, bad enum value, W out of range */
+    GEMM_RS_ERR_SHAPE = -2,       /* M % W, K % W, (K/W) % 8, N % 8, negative or too-large size */
+    GEMM_RS_ERR_ALIGN = -3,       /* a device pointer not 16-byte (workspace: 256-byte) aligned */
+    GEMM_RS_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (message has the detail) */
+    GEMM_RS_ERR_TIMEOUT = -5,     /* a device-side wait ran past its cycle limit */
+    GEMM_RS_ERR_UNSUPPORTED = -6, /* dtype combination or device (needs sm_103) not supported */
+    GEMM_RS_ERR_WORKSPACE = -7    /* workspace smaller than gemm_rs_workspace_bytes() */
+};
+
+/* Debug flags for gemm_rs_set_debug. */
+enum {
+    /* The TMA producer issues no loads, so the MMA warp's wait on the first
+     * stage runs out.  This exercises the timeout path on the GPU without a
+     * fault.  Use only together with a short gemm_rs_set_timeout_cycles. */
+    GEMM_RS_DEBUG_STALL_PRODUCER = 1
+};
+
+/*
+ * Bytes of device workspace that a handle with this shape needs.  This
+ * covers every tile width the library may pick.  Layout (internal, for
+ * information):
+ *   [0, 256)   device status word
+ *   flags      one uint32 arrival counter per output tile (ceil(M/128) x ceil(N/64) max)
+ *   partials   fp32 partial tiles, one per (output tile, rank), grouped by the chunk
+ *              that owns the tile's first row: W * ceil(M/128)*128 * ceil(N/256)*256 * 4 bytes
+ * Returns 0 for invalid arguments (same checks as gemm_rs_create).
+ */
+GEMM_RS_API size_t gemm_rs_workspace_bytes(int64_t M, int64_t N, int64_t K, int W);
+
+/*
+ * Create a handle for one problem shape.
+ *   M, N      output rows and columns.  M % W == 0 and N % 8 == 0.  M = 0 or
+ *             N = 0 gives an empty problem: run() then returns at once.
+ *   K         TOTAL reduction length.  Each rank holds K/W of it.  K % W == 0
+ *             and (K/W) % 8 == 0.  K = 0 gives Y = W * beta * C.
+ *   W         logical tensor-parallel ranks, 1 .. 16.
+ *   alpha, beta  epilogue scalars (see OPERATION).
+ *   ab_dtype  GEMM_RS_BF16 (A and B).
+ *   c_dtype   GEMM_RS_BF16.
+ *   y_dtype   GEMM_RS_BF16 or GEMM_RS_FP32.
+ *   workspace device, caller-owned, 256-byte aligned, at least
+ *             gemm_rs_workspace_bytes(M, N, K, W) bytes, workspace_bytes = its size.
+ *             It must stay valid until gemm_rs_destroy.  Its contents
+ *             belong to the library while the handle lives.
+ *   stream    create() zeroes the status word and the tile counters once, on this
+ *             stream, with one cudaMemsetAsync.  Later runs never clear them again.
+ * Fails with ERR_ARG / ERR_SHAPE / ERR_ALIGN / ERR_WORKSPACE / ERR_UNSUPPORTED /
+ * ERR_CUDA.  On failure *out is set to NULL.
+ */
+GEMM_RS_API int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W,
+                   float alpha, float beta, gemm_rs_dtype ab_dtype,
+                   gemm_rs_dtype c_dtype, gemm_rs_dtype y_dtype,
+                   void *workspace, size_t workspace_bytes, gemm_rs_stream_t stream);
+
+/*
+ * Run the fused kernel once.  It is asynchronous on `stream`: no host sync
+ * and no memset.
+ *   A  device, bf16 [W][M][K/W] row-major (K contiguous), 16-byte aligned.
+ *   B  device, bf16 [W][K/W][N] row-major (N contiguous), 16-byte aligned.
+ *   C  device, bf16 [M][N], 16-byte aligned.  May be NULL when beta == 0, and
+ *      is not read then.
+ *   Y  device, [M][N] in y_dtype, 16-byte aligned.  Rows [c*M/W, (c+1)*M/W)
+ *      are chunk c.  Every element is written.
+ * A and B may change between calls.  Their TMA descriptors are re-encoded on
+ * the host when the pointers change.  Returns ERR_ARG / ERR_ALIGN for bad
+ * pointers and ERR_CUDA if the launch fails.  A device-side timeout is not
+ * seen here: call gemm_rs_status.
+ */
+GEMM_RS_API int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
+                gemm_rs_stream_t stream);
+
+/* Free the handle's host state.  Does not touch device memory.  NULL is a no-op. */
+GEMM_RS_API int gemm_rs_destroy(gemm_rs_t h);
+
+/* Message for the last failing call on this thread ("" if none).  The string
+ * stays valid until the next failing call on this thread. */
+GEMM_RS_API const char *gemm_rs_last_error(void);
+
+/*
+ * Synchronise `stream`, then read and clear the handle's device status
+ * word.  Returns GEMM_RS_OK, or GEMM_RS_ERR_TIMEOUT if a kernel of this
+ * handle gave up on a wait since the last check.  After a timeout, Y of that
+ * run is incomplete and the tile counters may be non-zero: call
+ * gemm_rs_reset before the next run.
+ */
+GEMM_RS_API int gemm_rs_status(gemm_rs_t h, gemm_rs_stream_t stream);
+
+/* Zero the status word and the tile counters again (one cudaMemsetAsync on
+ * `stream`).  Needed only after a timeout. */
+GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
+
+/*
+ * The global tile order of the fused kernel, written to host memory `out` as
+ * int32 triples (r, mt, nt) for entries g = 0 .. W*nM*nN-1, where
+ * nM = ceil(M/bm) and nN = ceil(N/bn).  CTA b of a grid of G CTAs processes
+ * entries b, b+G, b+2G, ...
+ *   - Rank r visits its chunks in the order (r+1+s) mod W, s = 0 .. W-1:
+ *     the remote chunks first and its own chunk r last
+ *     ("flux实现：sm80 gemm+rs", section "gemmrs版本的swizzle如何编排").
+ *     Each rank's start is offset by its rank ("flux精读" §4.1), so at every
+ *     step the W ranks target W different chunks.
+ *   - A row tile belongs to the chunk of its first row.  Inside a chunk, a
+ *     rank walks the column tiles from offset (r*nN)/W.  For each column
+ *     tile, it takes the chunk's row tiles in ascending order.
+ *   - Entry p*W + r is rank r's p-th tile: the ranks advance side by side.
+ * `cap` is the capacity of `out` in triples.  Returns the number of entries,
+ * or a negative error code (ERR_SHAPE if cap is too small).
+ */
+GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *out, int64_t cap);
+
+/*
+ * Launch plan of the handle (host outputs; any pointer may be NULL):
+ *   bm, bn   the output tile (bm = 128; bn = 256, 128 or 64)
+ *   stages   depth of the TMA -> MMA shared-memory ring
+ *   grid     CTAs launched (persistent: one per SM, at most one per work item)
+ */
+GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid);
+
+/* Override the tile width (bn = 256, 128 or 64).  The default is picked so
+ * that there are at least four work items per SM.  Returns ERR_ARG for any
+ * other value. */
+GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
+
+/* Device wait limit in SM clock cycles (default 2^32, about two seconds).  A
+ * wait that runs past it sets the status word and lets the kernel exit. */
+GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
+
+/*
+ * Debug hooks.
+ *   record  device int32 buffer of 4 * W*nM*nN entries, or NULL.  When set,
+ *           each run writes (r, mt, nt, cta) for every entry g that it
+ *           processes, at record[4g .. 4g+3].
+ *   flags   GEMM_RS_DEBUG_* bits (0 = none).
+ */
+GEMM_RS_API int gemm_rs_set_debug(gemm_rs_t h, int32_t *record, int flags);
+
+/*
+ * Baseline only (not the fused path): the separate reduce step of an
+ * unfused GEMM+RS, which runs after W per-rank GEMMs.
+ *   partials  device, [W][M][N], fp32 (partial_dtype = GEMM_RS_FP32) or bf16
+ *   C         device bf16 [M][N], or NULL when beta == 0
+ *   Y         device [M][N] in y_dtype
+ * Y = fold over r in rank order of fp32(alpha * partials[r] + beta * C), with
+ * the same rounding as the fused path.  Asynchronous on `stream`.
+ * Pointers must be 16-byte aligned, and N % 8 == 0.
+ */
+GEMM_RS_API int gemm_rs_reduce_partials(const void *partials, gemm_rs_dtype partial_dtype, const void *C,
+                            void *Y, int64_t M, int64_t N, int W, float alpha, float beta,
+                            gemm_rs_dtype y_dtype, gemm_rs_stream_t stream);
+
+/* Library version string. */
+GEMM_RS_API const char *gemm_rs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_RS_H */

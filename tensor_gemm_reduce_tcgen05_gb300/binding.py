@@ -1,0 +1,251 @@
+"""ctypes binding of the C ABI in ``include/gemm_rs.h``.
+
+Each function has the C function's name and only marshals arguments.  Device
+pointers and streams are passed as Python ints (``tensor.data_ptr()``,
+``torch.cuda.Stream.cuda_stream``).  Every step of the computation runs in the
+CUDA library.  If the library is missing, :func:`lib` raises instead of
+falling back to anything else.
+
+:class:`GemmRS` is a convenience owner for a handle.  It keeps a torch-allocated
+workspace and accepts torch tensors.  PyTorch is used there only for device
+memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemm_rs.so")
+
+GEMM_RS_BF16 = 0
+GEMM_RS_FP32 = 1
+
+GEMM_RS_OK = 0
+GEMM_RS_ERR_ARG = -1
+GEMM_RS_ERR_SHAPE = -2
+GEMM_RS_ERR_ALIGN = -3
+GEMM_RS_ERR_CUDA = -4
+GEMM_RS_ERR_TIMEOUT = -5
+GEMM_RS_ERR_UNSUPPORTED = -6
+GEMM_RS_ERR_WORKSPACE = -7
+
+GEMM_RS_DEBUG_STALL_PRODUCER = 1
+
+_DTYPES = {"bf16": GEMM_RS_BF16, "fp32": GEMM_RS_FP32}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmRSError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"gemm_rs error {code}: {message}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m tensor_gemm_reduce_tcgen05_gb300.build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, f32, sz, vp = (ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                                 ctypes.c_void_p)
+        u64 = ctypes.c_uint64
+        sig = {
+            "gemm_rs_workspace_bytes": (sz, [i64, i64, i64, i32]),
+            "gemm_rs_create": (i32, [ctypes.POINTER(vp), i64, i64, i64, i32, f32, f32, i32, i32,
+                                     i32, vp, sz, vp]),
+            "gemm_rs_run": (i32, [vp, vp, vp, vp, vp, vp]),
+            "gemm_rs_destroy": (i32, [vp]),
+            "gemm_rs_last_error": (ctypes.c_char_p, []),
+            "gemm_rs_status": (i32, [vp, vp]),
+            "gemm_rs_reset": (i32, [vp, vp]),
+            "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, vp, i64]),
+            "gemm_rs_get_plan": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+            "gemm_rs_set_tile_n": (i32, [vp, i32]),
+            "gemm_rs_set_timeout_cycles": (i32, [vp, u64]),
+            "gemm_rs_set_debug": (i32, [vp, vp, i32]),
+            "gemm_rs_reduce_partials": (i32, [vp, i32, vp, vp, i64, i64, i32, f32, f32, i32, vp]),
+            "gemm_rs_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def gemm_rs_last_error() -> str:
+    return lib().gemm_rs_last_error().decode()
+
+
+def _check(rc: int) -> int:
+    if rc < 0:
+        raise GemmRSError(rc, gemm_rs_last_error())
+    return rc
+
+
+def gemm_rs_version() -> str:
+    return lib().gemm_rs_version().decode()
+
+
+def gemm_rs_workspace_bytes(M: int, N: int, K: int, W: int) -> int:
+    return int(lib().gemm_rs_workspace_bytes(M, N, K, W))
+
+
+def gemm_rs_create(M, N, K, W, alpha, beta, ab_dtype, c_dtype, y_dtype, workspace,
+                   workspace_bytes, stream=0) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().gemm_rs_create(ctypes.byref(h), M, N, K, W, alpha, beta, ab_dtype, c_dtype,
+                                y_dtype, workspace, workspace_bytes, stream))
+    return h
+
+
+def gemm_rs_run(h, A, B, C, Y, stream=0) -> None:
+    _check(lib().gemm_rs_run(h, A, B, C, Y, stream))
+
+
+def gemm_rs_destroy(h) -> None:
+    _check(lib().gemm_rs_destroy(h))
+
+
+def gemm_rs_status(h, stream=0) -> int:
+    """Synchronises the stream.  Returns GEMM_RS_OK or GEMM_RS_ERR_TIMEOUT
+    (other codes raise)."""
+    rc = lib().gemm_rs_status(h, stream)
+    if rc in (GEMM_RS_OK, GEMM_RS_ERR_TIMEOUT):
+        return rc
+    return _check(rc)
+
+
+def gemm_rs_reset(h, stream=0) -> None:
+    _check(lib().gemm_rs_reset(h, stream))
+
+
+def gemm_rs_schedule(M: int, N: int, W: int, bm: int, bn: int) -> np.ndarray:
+    nM, nN = -(-M // bm), -(-N // bn)
+    out = np.zeros((W * nM * nN, 3), dtype=np.int32)
+    n = _check(lib().gemm_rs_schedule(M, N, W, bm, bn, out.ctypes.data, out.shape[0]))
+    return out[:n]
+
+
+def gemm_rs_get_plan(h) -> dict:
+    v = [ctypes.c_int() for _ in range(4)]
+    _check(lib().gemm_rs_get_plan(h, *[ctypes.byref(x) for x in v]))
+    return dict(zip(("bm", "bn", "stages", "grid"), (x.value for x in v)))
+
+
+def gemm_rs_set_tile_n(h, bn: int) -> None:
+    _check(lib().gemm_rs_set_tile_n(h, bn))
+
+
+def gemm_rs_set_timeout_cycles(h, cycles: int) -> None:
+    _check(lib().gemm_rs_set_timeout_cycles(h, cycles))
+
+
+def gemm_rs_set_debug(h, record=0, flags: int = 0) -> None:
+    _check(lib().gemm_rs_set_debug(h, record, flags))
+
+
+def gemm_rs_reduce_partials(partials, partial_dtype, C, Y, M, N, W, alpha, beta, y_dtype,
+                            stream=0) -> None:
+    _check(lib().gemm_rs_reduce_partials(partials, partial_dtype, C, Y, M, N, W, alpha, beta,
+                                         y_dtype, stream))
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class GemmRS:
+    """Owns one handle and its workspace (a torch uint8 CUDA tensor).
+
+    Y = sum over r of (alpha * A[r] @ B[r] + beta * C), as W chunks of M/W rows.
+    A is bf16 [W, M, K/W], B is bf16 [W, K/W, N], C is bf16 [M, N] (or None when
+    beta == 0), and Y is [M, N] in y_dtype.
+    """
+
+    def __init__(self, M: int, N: int, K: int, W: int, alpha: float = 1.0, beta: float = 0.0,
+                 y_dtype: str = "bf16", device=None, stream=None, tile_n: int | None = None):
+        import torch
+        lib()
+        self.M, self.N, self.K, self.W = M, N, K, W
+        self.alpha, self.beta, self.y_dtype = alpha, beta, y_dtype
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        nbytes = gemm_rs_workspace_bytes(M, N, K, W)
+        if nbytes == 0:
+            _check(GEMM_RS_ERR_SHAPE)
+        with torch.cuda.device(self.device):
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            self.handle = gemm_rs_create(M, N, K, W, alpha, beta, GEMM_RS_BF16, GEMM_RS_BF16,
+                                         _DTYPES[y_dtype], self.workspace.data_ptr(), nbytes,
+                                         _stream_ptr(stream))
+        if tile_n is not None:
+            gemm_rs_set_tile_n(self.handle, tile_n)
+
+    @property
+    def plan(self) -> dict:
+        return gemm_rs_get_plan(self.handle)
+
+    def new_output(self):
+        import torch
+        dt = torch.bfloat16 if self.y_dtype == "bf16" else torch.float32
+        return torch.empty((self.M, self.N), dtype=dt, device=self.device)
+
+    def run(self, A, B, C=None, Y=None, stream=None):
+        """Launch once (asynchronous).  Returns Y."""
+        import torch
+        for t, name in ((A, "A"), (B, "B")):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"{name} must be a contiguous bf16 tensor on {self.device}")
+        if tuple(A.shape) != (self.W, self.M, self.K // self.W):
+            raise ValueError(f"A must be [W, M, K/W] = {(self.W, self.M, self.K // self.W)}")
+        if tuple(B.shape) != (self.W, self.K // self.W, self.N):
+            raise ValueError(f"B must be [W, K/W, N] = {(self.W, self.K // self.W, self.N)}")
+        if C is not None and (C.dtype != torch.bfloat16 or not C.is_contiguous()
+                              or tuple(C.shape) != (self.M, self.N)):
+            raise ValueError("C must be a contiguous bf16 [M, N] tensor")
+        if Y is None:
+            Y = self.new_output()
+        gemm_rs_run(self.handle, A.data_ptr(), B.data_ptr(), 0 if C is None else C.data_ptr(),
+                    Y.data_ptr(), _stream_ptr(stream))
+        return Y
+
+    def status(self, stream=None) -> int:
+        return gemm_rs_status(self.handle, _stream_ptr(stream))
+
+    def reset(self, stream=None) -> None:
+        gemm_rs_reset(self.handle, _stream_ptr(stream))
+
+    def flags_view(self):
+        """The tile counters (a view into the workspace), for tests."""
+        import torch
+        nM, nN = -(-self.M // 128), -(-self.N // 64)
+        return self.workspace[256:256 + 4 * nM * nN].view(torch.int32)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            gemm_rs_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,517 @@
+// Host side of the C ABI declared in include/gemm_rs.h: argument checks, the
+// workspace layout, TMA descriptors, the launch plan and the launch.  No
+// exception crosses the boundary; errors come back as codes, and the
+// message is kept per thread.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <new>
+#include <string>
+
+#include "gemm_rs.h"
+#include "gemm_rs_kernel.cuh"
+#include "reduce_baseline.cuh"
+#include "schedule.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(GEMM_RS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr size_t kStatusBytes = 256;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Layout {
+    size_t flags_off, flags_bytes, part_off, part_bytes, total;
+};
+
+Layout layout_for(int64_t M, int64_t N, int W)
+{
+    Layout L;
+    const int64_t nM = cdiv(M, gemm_rs::kBM);
+    L.flags_off = kStatusBytes;
+    L.flags_bytes = round_up(static_cast<size_t>(nM * cdiv(N, 64)) * sizeof(uint32_t), 256);
+    L.part_off = L.flags_off + L.flags_bytes;
+    L.part_bytes = static_cast<size_t>(W) * static_cast<size_t>(nM) * gemm_rs::kBM *
+                   static_cast<size_t>(cdiv(N, 256) * 256) * sizeof(float);
+    L.total = L.part_off + L.part_bytes;
+    return L;
+}
+
+int check_shape(int64_t M, int64_t N, int64_t K, int W)
+{
+    if (W < 1 || W > 16)
+        return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_RS_ERR_SHAPE, "negative size (M=%lld N=%lld K=%lld)", (long long)M,
+                    (long long)N, (long long)K);
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return fail(GEMM_RS_ERR_SHAPE, "size above 2^31-1");
+    if (M % W != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "M = %lld is not a multiple of W = %d (chunks are M/W rows)",
+                    (long long)M, W);
+    if (K % W != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "K = %lld is not a multiple of W = %d", (long long)K, W);
+    if ((K / W) % 8 != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "K/W = %lld is not a multiple of 8 (16-byte TMA row stride)",
+                    (long long)(K / W));
+    if (N % 8 != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "N = %lld is not a multiple of 8 (16-byte rows)",
+                    (long long)N);
+    return GEMM_RS_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiled *out)
+{
+    static EncodeTiled fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+            return fail(GEMM_RS_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    *out = fn;
+    return GEMM_RS_OK;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
+int encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint32_t b0, uint32_t b1)
+{
+    EncodeTiled enc;
+    int rc = get_encoder(&enc);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_RS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return GEMM_RS_OK;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool attrs_set = false;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+
+template <int BN>
+cudaError_t set_kernel_attrs()
+{
+    return cudaFuncSetAttribute(gemm_rs::gemm_rs_fused_kernel<BN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemm_rs::smem_bytes<BN>());
+}
+
+int prepare_device(int *dev_out, int *sms_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.attrs_set) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+        if (major != 10 || minor != 3)
+            return fail(GEMM_RS_ERR_UNSUPPORTED,
+                        "device %d has compute capability %d.%d; this library is built for sm_103a",
+                        dev, major, minor);
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        if ((e = set_kernel_attrs<256>()) != cudaSuccess ||
+            (e = set_kernel_attrs<128>()) != cudaSuccess ||
+            (e = set_kernel_attrs<64>()) != cudaSuccess)
+            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        d.attrs_set = true;
+    }
+    *dev_out = dev;
+    *sms_out = d.sms;
+    return GEMM_RS_OK;
+}
+
+int stages_for(int bn)
+{
+    switch (bn) {
+    case 256: return gemm_rs::TileCfg<256>::kStages;
+    case 128: return gemm_rs::TileCfg<128>::kStages;
+    default: return gemm_rs::TileCfg<64>::kStages;
+    }
+}
+
+// The widest tile that still gives at least four work items per SM.
+int pick_bn(int64_t M, int64_t N, int W, int sms)
+{
+    const int64_t nM = cdiv(M, gemm_rs::kBM);
+    for (int bn : {256, 128}) {
+        if (static_cast<int64_t>(W) * nM * cdiv(N, bn) >= 4LL * sms)
+            return bn;
+    }
+    return 64;
+}
+
+} // namespace
+
+struct gemm_rs_s {
+    int64_t M, N, K, Kpr;
+    int W;
+    float alpha, beta;
+    gemm_rs_dtype y_dtype;
+    uint8_t *ws;
+    Layout L;
+    int device, sms, bn;
+    CUtensorMap tmA, tmB;
+    const void *tmA_ptr, *tmB_ptr;
+    unsigned long long timeout;
+    int32_t *record;
+    int debug_flags;
+};
+
+extern "C" {
+
+const char *gemm_rs_version(void) { return "gemm_rs 0.1 (sm_103a, tcgen05)"; }
+
+const char *gemm_rs_last_error(void) { return g_err.c_str(); }
+
+size_t gemm_rs_workspace_bytes(int64_t M, int64_t N, int64_t K, int W)
+{
+    if (check_shape(M, N, K, W) != GEMM_RS_OK)
+        return 0;
+    return layout_for(M, N, W).total;
+}
+
+int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float alpha, float beta,
+                   gemm_rs_dtype ab_dtype, gemm_rs_dtype c_dtype, gemm_rs_dtype y_dtype,
+                   void *workspace, size_t workspace_bytes, gemm_rs_stream_t stream)
+{
+    if (out == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = check_shape(M, N, K, W);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    if (ab_dtype != GEMM_RS_BF16)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "A/B dtype must be GEMM_RS_BF16");
+    if (c_dtype != GEMM_RS_BF16)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "C dtype must be GEMM_RS_BF16");
+    if (y_dtype != GEMM_RS_BF16 && y_dtype != GEMM_RS_FP32)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "Y dtype must be GEMM_RS_BF16 or GEMM_RS_FP32");
+    if (!(alpha == alpha) || !(beta == beta))
+        return fail(GEMM_RS_ERR_ARG, "alpha and beta must not be NaN");
+    const Layout L = layout_for(M, N, W);
+    if (workspace == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "workspace is NULL");
+    if (!aligned(workspace, 256))
+        return fail(GEMM_RS_ERR_ALIGN, "workspace must be 256-byte aligned");
+    if (workspace_bytes < L.total)
+        return fail(GEMM_RS_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                    L.total);
+    int dev = 0, sms = 0;
+    if ((rc = prepare_device(&dev, &sms)) != GEMM_RS_OK)
+        return rc;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, L.part_off, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(status and tile counters)");
+    gemm_rs_s *h = new (std::nothrow) gemm_rs_s();
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "out of host memory");
+    h->M = M;
+    h->N = N;
+    h->K = K;
+    h->Kpr = K / W;
+    h->W = W;
+    h->alpha = alpha;
+    h->beta = beta;
+    h->y_dtype = y_dtype;
+    h->ws = static_cast<uint8_t *>(workspace);
+    h->L = L;
+    h->device = dev;
+    h->sms = sms;
+    h->bn = pick_bn(M, N, W, sms);
+    h->tmA_ptr = h->tmB_ptr = nullptr;
+    h->timeout = 1ull << 32;
+    h->record = nullptr;
+    h->debug_flags = 0;
+    *out = h;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_destroy(gemm_rs_t h)
+{
+    delete h;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    const int64_t total = static_cast<int64_t>(h->W) * cdiv(h->M, gemm_rs::kBM) * cdiv(h->N, h->bn);
+    if (bm)
+        *bm = gemm_rs::kBM;
+    if (bn)
+        *bn = h->bn;
+    if (stages)
+        *stages = stages_for(h->bn);
+    if (grid)
+        *grid = static_cast<int>(total < h->sms ? total : h->sms);
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_tile_n(gemm_rs_t h, int bn)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (bn != 64 && bn != 128 && bn != 256)
+        return fail(GEMM_RS_ERR_ARG, "tile width %d is not 64, 128 or 256", bn);
+    h->bn = bn;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (cycles == 0)
+        return fail(GEMM_RS_ERR_ARG, "timeout must be positive");
+    h->timeout = cycles;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_debug(gemm_rs_t h, int32_t *record, int flags)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (flags & ~GEMM_RS_DEBUG_STALL_PRODUCER)
+        return fail(GEMM_RS_ERR_ARG, "unknown debug flags 0x%x", flags);
+    if (record != nullptr && !aligned(record, 16))
+        return fail(GEMM_RS_ERR_ALIGN, "record buffer must be 16-byte aligned");
+    h->record = record;
+    h->debug_flags = flags;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
+                gemm_rs_stream_t stream)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (h->M == 0 || h->N == 0)
+        return GEMM_RS_OK;
+    if (Y == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "Y is NULL");
+    if (!aligned(Y, 16))
+        return fail(GEMM_RS_ERR_ALIGN, "Y must be 16-byte aligned");
+    if (h->beta != 0.0f) {
+        if (C == nullptr)
+            return fail(GEMM_RS_ERR_ARG, "C is NULL but beta != 0");
+        if (!aligned(C, 16))
+            return fail(GEMM_RS_ERR_ALIGN, "C must be 16-byte aligned");
+    }
+    if (h->Kpr > 0) {
+        if (A == nullptr || B == nullptr)
+            return fail(GEMM_RS_ERR_ARG, "A or B is NULL");
+        if (!aligned(A, 16) || !aligned(B, 16))
+            return fail(GEMM_RS_ERR_ALIGN, "A and B must be 16-byte aligned");
+        int rc;
+        if (A != h->tmA_ptr) {
+            // A: [W][M][K/W] -> dims {K/W, M, W}, box {64, 128, 1}
+            if ((rc = encode_3d(&h->tmA, A, h->Kpr, h->M, h->W, gemm_rs::kBK, gemm_rs::kBM)) != GEMM_RS_OK)
+                return rc;
+            h->tmA_ptr = A;
+        }
+        if (B != h->tmB_ptr) {
+            // B: [W][K/W][N] -> dims {N, K/W, W}, box {64, 64, 1}
+            if ((rc = encode_3d(&h->tmB, B, h->N, h->Kpr, h->W, 64, gemm_rs::kBK)) != GEMM_RS_OK)
+                return rc;
+            h->tmB_ptr = B;
+        }
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev != h->device)
+        return fail(GEMM_RS_ERR_ARG, "handle was created on device %d, current device is %d",
+                    h->device, dev);
+
+    gemm_rs::KernelArgs a;
+    a.W = h->W;
+    a.M = static_cast<int>(h->M);
+    a.N = static_cast<int>(h->N);
+    a.nM = static_cast<int>(cdiv(h->M, gemm_rs::kBM));
+    a.nN = static_cast<int>(cdiv(h->N, h->bn));
+    a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
+    a.R = h->M / h->W;
+    a.total = static_cast<int64_t>(h->W) * a.nM * a.nN;
+    a.alpha = h->alpha;
+    a.beta = h->beta;
+    a.C = h->beta != 0.0f ? static_cast<const uint16_t *>(C) : nullptr;
+    a.Y = Y;
+    a.y_fp32 = h->y_dtype == GEMM_RS_FP32 ? 1 : 0;
+    a.part = reinterpret_cast<float *>(h->ws + h->L.part_off);
+    a.flags = reinterpret_cast<uint32_t *>(h->ws + h->L.flags_off);
+    a.status = reinterpret_cast<uint32_t *>(h->ws);
+    a.record = h->record;
+    a.timeout = h->timeout;
+    a.stall_producer = (h->debug_flags & GEMM_RS_DEBUG_STALL_PRODUCER) ? 1 : 0;
+
+    const int grid = static_cast<int>(a.total < h->sms ? a.total : h->sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (h->bn) {
+    case 256:
+        gemm_rs::gemm_rs_fused_kernel<256>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<256>(), s>>>(h->tmA, h->tmB, a);
+        break;
+    case 128:
+        gemm_rs::gemm_rs_fused_kernel<128>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<128>(), s>>>(h->tmA, h->tmB, a);
+        break;
+    default:
+        gemm_rs::gemm_rs_fused_kernel<64>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<64>(), s>>>(h->tmA, h->tmB, a);
+        break;
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the fused GEMM+RS kernel");
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_status(gemm_rs_t h, gemm_rs_stream_t stream)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, h->ws, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the status word");
+    if (word == 0)
+        return GEMM_RS_OK;
+    e = cudaMemsetAsync(h->ws, 0, sizeof word, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "clearing the status word");
+    static const char *role[] = {"?", "TMA producer", "MMA issuer", "epilogue", "reducer"};
+    return fail(GEMM_RS_ERR_TIMEOUT, "device wait timed out in the %s (status %u)",
+                role[word < 5 ? word : 0], word);
+}
+
+int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    cudaError_t e = cudaMemsetAsync(h->ws, 0, h->L.part_off, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(status and tile counters)");
+    return GEMM_RS_OK;
+}
+
+int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *out, int64_t cap)
+{
+    if (W < 1 || W > 16)
+        return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
+    if (M < 1 || N < 1 || M % W != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "need M, N >= 1 and M %% W == 0");
+    if (bm != gemm_rs::kBM || (bn != 64 && bn != 128 && bn != 256))
+        return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not a tile of this library", bm, bn);
+    if (out == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "out is NULL");
+    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), static_cast<int>(cdiv(N, bn)), 7, M / W};
+    const int64_t total = static_cast<int64_t>(W) * s.nM * s.nN;
+    if (cap < total)
+        return fail(GEMM_RS_ERR_SHAPE, "cap %lld < %lld entries", (long long)cap, (long long)total);
+    for (int64_t g = 0; g < total; ++g) {
+        int r, mt, nt;
+        gemm_rs::decode_tile(s, g, r, mt, nt);
+        out[3 * g] = r;
+        out[3 * g + 1] = mt;
+        out[3 * g + 2] = nt;
+    }
+    return total;
+}
+
+int gemm_rs_reduce_partials(const void *partials, gemm_rs_dtype partial_dtype, const void *C,
+                            void *Y, int64_t M, int64_t N, int W, float alpha, float beta,
+                            gemm_rs_dtype y_dtype, gemm_rs_stream_t stream)
+{
+    if (W < 1 || W > 16)
+        return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
+    if (M < 0 || N < 0 || N % 8 != 0)
+        return fail(GEMM_RS_ERR_SHAPE, "need M, N >= 0 and N %% 8 == 0");
+    if ((partial_dtype != GEMM_RS_BF16 && partial_dtype != GEMM_RS_FP32) ||
+        (y_dtype != GEMM_RS_BF16 && y_dtype != GEMM_RS_FP32))
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "unknown dtype");
+    if (M == 0 || N == 0)
+        return GEMM_RS_OK;
+    if (partials == nullptr || Y == nullptr || (beta != 0.0f && C == nullptr))
+        return fail(GEMM_RS_ERR_ARG, "NULL partials, Y, or C with beta != 0");
+    if (!aligned(partials, 16) || !aligned(Y, 16) || (beta != 0.0f && !aligned(C, 16)))
+        return fail(GEMM_RS_ERR_ALIGN, "pointers must be 16-byte aligned");
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "querying the device");
+    gemm_rs::ReduceArgs a{partials, partial_dtype == GEMM_RS_BF16 ? 1 : 0,
+                          beta != 0.0f ? static_cast<const uint16_t *>(C) : nullptr, Y,
+                          y_dtype == GEMM_RS_FP32 ? 1 : 0, M, N, W, alpha, beta};
+    const int64_t groups = M * (N / 8);
+    int64_t blocks = (groups + 255) / 256;
+    if (blocks > int64_t(sms) * 8)
+        blocks = int64_t(sms) * 8;
+    e = gemm_rs::launch_reduce_partials(a, static_cast<int>(blocks),
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the baseline reduce kernel");
+    return GEMM_RS_OK;
+}
+
+} // extern "C"

@@ -1,0 +1,537 @@
+// The fused GEMM + reduce-scatter kernel for sm_103a.
+//
+// One persistent CTA per SM walks the global tile order of schedule.cuh.
+// Each work item is one rank-tile (r, mt, nt): the 128 x BN output tile
+// (mt, nt) of logical rank r's GEMM A_r * B_r over its K/W shard.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer (one thread).  For each k-block, it loads the
+//               A_r box [128 x 64] and the B_r boxes [64 x 64] (BN/64 of
+//               them) into a stage of the shared-memory ring, 128-byte
+//               swizzled, and completes the stage's `full` mbarrier.
+//   warp 1      TMEM allocator and MMA issuer (one thread).  It issues
+//               tcgen05.mma (M = 128, N = BN, K = 16, bf16 -> fp32) into one of
+//               two TMEM accumulators of BN columns each.  tcgen05.commit
+//               frees each stage, and at the end of the tile signals
+//               `acc_full`.
+//   warps 2-5   epilogue visitor.  Each warp drains 32 TMEM lanes (one row
+//               per thread), computes p = alpha*acc + beta*C
+//               ("flux实现：sm80 gemm+rs", section "custom_evt_d()"), and
+//               stores p with 16-byte coalesced stores into the tile's
+//               rank-r slot of the chunk workspace ("evt_store_d()": the
+//               store goes to the reduce-scatter buffer, not to Y).  It then
+//               increments the tile's 32-bit arrival counter.  The rank that
+//               arrives last resets the counter to 0 and queues the tile for
+//               the reducers.
+//   warps 6-9   reducers.  For each queued tile they fold the W partials in
+//               rank order in fp32, convert, and write Y.  They run beside
+//               the epilogue, so a reduction never holds a TMEM accumulator.
+//
+// There are no waits between CTAs.  The last arriver never waits for
+// anyone, so the kernel cannot deadlock however many CTAs it has (the
+// deadlock of a device-wide barrier with more CTAs than fit at once is
+// described in "flux实现：sm80 gemm+rs", section "device side barrier").
+// Every mbarrier wait is bounded in SM cycles.  A wait that runs out records
+// a code in the status word, and the CTA then drains its TMA loads and MMAs
+// and exits.
+//
+// Partial slot layout: slot (tile, r) holds 4 x (BN/32) blocks of 32 rows x 32
+// columns (fp32).  Inside a block, float4 j (columns 4j .. 4j+3) of row t is
+// at float4 index j*32 + t, so each warp-wide 16-byte store or load covers 512
+// contiguous bytes.  Slots are ordered by row tile, so the slots of the tiles
+// keyed to one chunk form one contiguous region: the chunk's workspace.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace gemm_rs {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 320;
+constexpr int kEpiWarp0 = 2;
+constexpr int kRedWarp0 = 6;
+constexpr int kRQ = 16;          // depth of the reduce queue
+constexpr uint32_t kBarEpi = 1;  // named barrier of the 128 epilogue threads
+constexpr int kMaxStages = 8;
+
+// Status word codes (first failure wins).
+enum : uint32_t {
+    kStatusOk = 0,
+    kStatusTimeoutProducer = 1,
+    kStatusTimeoutMma = 2,
+    kStatusTimeoutEpilogue = 3,
+    kStatusTimeoutReducer = 4,
+};
+
+template <int BN>
+struct TileCfg {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "BN must be 64, 128 or 256");
+    static constexpr int kABytes = kBM * kBK * 2;            // 16 KB
+    static constexpr int kBBytes = BN * kBK * 2;             // BN/64 boxes of 8 KB
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kTmemCols = 2 * BN;                 // two accumulators
+    static constexpr int kSlabs = BN / 32;
+    static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, BN, false, true);
+    static constexpr int64_t kSlotFloats = int64_t(kBM) * BN; // one partial tile
+    static_assert(kStages <= kMaxStages, "too many stages");
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+struct KernelArgs {
+    int W, M, N, nM, nN, nK;
+    int64_t R;      // rows per chunk
+    int64_t total;  // W * nM * nN work items
+    float alpha, beta;
+    const uint16_t *C; // bf16 bits, NULL when beta == 0
+    void *Y;
+    int y_fp32;
+    float *part;
+    uint32_t *flags;
+    uint32_t *status;
+    int32_t *record;
+    unsigned long long timeout;
+    int stall_producer;
+};
+
+struct SmemCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t rq_full[kRQ];
+    uint64_t rq_empty[kRQ];
+    uint64_t drain;
+    int32_t rq_tile[kRQ];
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int BN>
+constexpr int smem_bytes()
+{
+    return 1024 + TileCfg<BN>::kStages * TileCfg<BN>::kStageBytes + int(sizeof(SmemCtl));
+}
+
+__device__ __forceinline__ void report(const KernelArgs &a, SmemCtl *ctl, uint32_t code)
+{
+    // The first role to fail records its code.  Roles that fail only because
+    // another role aborted leave the code alone.
+    if (*reinterpret_cast<volatile int *>(&ctl->abort) == 0)
+        atomicCAS(a.status, 0u, code);
+    *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+}
+
+// ------------------------------------------------------------------ producer
+template <int BN>
+__device__ __forceinline__ void run_producer(const KernelArgs &a, const Sched &sch,
+                                             const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                             uint8_t *smem, SmemCtl *ctl)
+{
+    using Cfg = TileCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    const uint64_t pol = ptx::policy_evict_normal();
+    uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    if (!a.stall_producer) {
+        for (int64_t g = blockIdx.x; g < a.total && ok; g += gridDim.x) {
+            int r, mt, nt;
+            decode_tile(sch, g, r, mt, nt);
+            if (a.record != nullptr) {
+                int32_t *rec = a.record + 4 * g;
+                rec[0] = r;
+                rec[1] = mt;
+                rec[2] = nt;
+                rec[3] = static_cast<int32_t>(blockIdx.x);
+            }
+            for (int kb = 0; kb < a.nK; ++kb) {
+                if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,
+                                    abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = ptx::smem_u32(&ctl->full[stage]);
+                ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+                const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
+                ptx::tma_load_3d(sa, tmA, fb, kb * kBK, mt * kBM, r, pol);
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j)
+                    ptx::tma_load_3d(sa + Cfg::kABytes + j * 8192, tmB, fb, nt * BN + j * 64,
+                                     kb * kBK, r, pol);
+                ++issued;
+                if (++stage == Cfg::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (ok) {
+        // Tail: wait until the MMA warp has released every stage, so that
+        // every tcgen05.commit arrival on this CTA's barriers has landed
+        // before the CTA exits.
+        for (int i = 0; i < Cfg::kStages; ++i) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,
+                                abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        report(a, ctl, kStatusTimeoutProducer);
+        // Drain: the most recent fill of each stage must have landed before
+        // the CTA's shared memory is released.
+        const int64_t n = issued < Cfg::kStages ? issued : Cfg::kStages;
+        for (int64_t i = 1; i <= n; ++i) {
+            const int64_t pos = issued - i;
+            const uint32_t s = static_cast<uint32_t>(pos % Cfg::kStages);
+            const uint32_t ph = static_cast<uint32_t>((pos / Cfg::kStages) & 1);
+            ptx::mbar_wait(ptx::smem_u32(&ctl->full[s]), ph, a.timeout, nullptr);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int BN>
+__device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint8_t *smem,
+                                        SmemCtl *ctl)
+{
+    using Cfg = TileCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int it = 0;
+    for (int64_t g = blockIdx.x; g < a.total; g += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!ptx::mbar_wait(ptx::smem_u32(&ctl->acc_empty[buf]), aph ^ 1u, a.timeout, abort_flag)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < a.nK; ++kb) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&ctl->full[stage]), phase, a.timeout, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
+            const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                // A: K-major, rows of 128 bytes, 8-row groups 1024 bytes apart;
+                //    K step of 16 elements = 32 bytes inside the swizzle atom.
+                // B: MN-major, 64-column atoms 8192 bytes apart (LBO), 8-row K
+                //    groups 1024 bytes apart (SBO); K step of 16 rows = 2048 bytes.
+                const uint64_t ad = ptx::sdesc_sw128(sa + kk * 32, 0, 1024);
+                const uint64_t bd = ptx::sdesc_sw128(sb + kk * 2048, 8192, 1024);
+                ptx::mma_bf16_ss(d, ad, bd, Cfg::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(ptx::smem_u32(&ctl->empty[stage]));
+            if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok)
+            break;
+        if (a.nK > 0)
+            ptx::mma_commit(ptx::smem_u32(&ctl->acc_full[buf]));
+        else
+            ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_full[buf]));
+    }
+    if (!ok) {
+        report(a, ctl, kStatusTimeoutMma);
+        // Drain every MMA issued so far before TMEM is freed.
+        ptx::mma_commit(ptx::smem_u32(&ctl->drain));
+        ptx::mbar_wait(ptx::smem_u32(&ctl->drain), 0u, a.timeout, nullptr);
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// ------------------------------------------------------------------ epilogue
+template <int BN>
+__device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &sch, uint32_t tmem,
+                                             SmemCtl *ctl, int warp, int lane)
+{
+    using Cfg = TileCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    const int q = warp & 3;                           // TMEM lanes [32q, 32q + 32)
+    const int etid = threadIdx.x - kEpiWarp0 * 32;    // 0 .. 127
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    uint32_t rq_n = 0;
+    int it = 0;
+    for (int64_t g = blockIdx.x; g < a.total; g += gridDim.x, ++it) {
+        int r, mt, nt;
+        decode_tile(sch, g, r, mt, nt);
+        const int buf = it & 1;
+        const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        const bool waited =
+            ptx::mbar_wait(ptx::smem_u32(&ctl->acc_full[buf]), aph, a.timeout, abort_flag);
+        if (ptx::named_bar_or(kBarEpi, 128, !(waited && ok))) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+
+        const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+        const bool row_ok = m < a.M;
+        float *slot = a.part + ((static_cast<int64_t>(mt) * a.nN + nt) * a.W + r) * Cfg::kSlotFloats +
+                      static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
+#pragma unroll 1
+        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
+            uint32_t v[32];
+            if (a.nK > 0) {
+                ptx::tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(buf * BN + slab * 32),
+                                        v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = 0u;
+            }
+            if (slab == Cfg::kSlabs - 1) {
+                // The accumulator is fully read: hand it back to the MMA warp.
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty[buf]));
+            }
+            float p[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                p[i] = a.alpha * __uint_as_float(v[i]);
+            if (a.beta != 0.0f) {
+                const int64_t n0 = static_cast<int64_t>(nt) * BN + slab * 32;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int64_t n = n0 + 8 * g8;
+                    if (row_ok && n < a.N) {
+                        const uint4 c = ptx::ld_nc_u4(a.C + m * a.N + n);
+                        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            p[8 * g8 + 2 * e] = fmaf(a.beta, bf16_lo(cw[e]), p[8 * g8 + 2 * e]);
+                            p[8 * g8 + 2 * e + 1] =
+                                fmaf(a.beta, bf16_hi(cw[e]), p[8 * g8 + 2 * e + 1]);
+                        }
+                    }
+                }
+            }
+            float *dst = slot + slab * 1024;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ptx::st_f4(dst + j * 128, make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+        }
+
+        // Every epilogue thread has issued its stores.  Publish them at gpu
+        // scope and count this rank in.
+        ptx::named_bar_sync(kBarEpi, 128);
+        if (etid == 0) {
+            __threadfence();
+            uint32_t *flag = a.flags + static_cast<int64_t>(mt) * a.nN + nt;
+            const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
+            if (old == static_cast<uint32_t>(a.W - 1)) {
+                // Last arriver: the counter goes back to 0 for the next call
+                // (no memset), and the tile goes to the reducers.
+                ptx::st_relaxed_gpu(flag, 0u);
+                const uint32_t s = rq_n % kRQ;
+                const uint32_t ph = (rq_n / kRQ) & 1u;
+                if (ptx::mbar_wait(ptx::smem_u32(&ctl->rq_empty[s]), ph ^ 1u, a.timeout, abort_flag)) {
+                    ctl->rq_tile[s] = mt * a.nN + nt;
+                    ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_full[s]));
+                    ++rq_n;
+                } else {
+                    ok = false;
+                }
+            }
+        }
+    }
+    if (etid == 0) {
+        if (ok) {
+            const uint32_t s = rq_n % kRQ;
+            const uint32_t ph = (rq_n / kRQ) & 1u;
+            if (ptx::mbar_wait(ptx::smem_u32(&ctl->rq_empty[s]), ph ^ 1u, a.timeout, abort_flag)) {
+                ctl->rq_tile[s] = -1; // no more tiles
+                ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_full[s]));
+            } else {
+                ok = false;
+            }
+        }
+        if (!ok)
+            report(a, ctl, kStatusTimeoutEpilogue);
+    }
+}
+
+// ------------------------------------------------------------------ reducer
+template <int BN>
+__device__ __forceinline__ void run_reducer(const KernelArgs &a, SmemCtl *ctl, int warp, int lane)
+{
+    using Cfg = TileCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    const int q = warp - kRedWarp0; // rows [32q, 32q + 32) of the tile
+    uint32_t n_jobs = 0;
+    while (true) {
+        const uint32_t s = n_jobs % kRQ;
+        const uint32_t ph = (n_jobs / kRQ) & 1u;
+        int waited = 1;
+        if (lane == 0)
+            waited = ptx::mbar_wait(ptx::smem_u32(&ctl->rq_full[s]), ph, a.timeout, abort_flag) ? 1 : 0;
+        waited = __shfl_sync(0xffffffffu, waited, 0);
+        if (!waited) {
+            if (lane == 0)
+                report(a, ctl, kStatusTimeoutReducer);
+            break;
+        }
+        const int tile = *reinterpret_cast<volatile int32_t *>(&ctl->rq_tile[s]);
+        if (tile < 0)
+            break;
+        const int mt = tile / a.nN;
+        const int nt = tile - mt * a.nN;
+        const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+        const bool row_ok = m < a.M;
+        const float *base = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
+                            static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
+#pragma unroll 1
+        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
+            const float *sb = base + slab * 1024;
+#pragma unroll 1
+            for (int jp = 0; jp < 4; ++jp) {
+                // Columns 8jp .. 8jp+7 of the slab: float4 j = 2jp and 2jp+1.
+                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+                for (int r0 = 0; r0 < a.W; r0 += 8) {
+                    float4 u0[8], u1[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (r0 + u < a.W) {
+                            const float *pp = sb + static_cast<int64_t>(r0 + u) * Cfg::kSlotFloats +
+                                              (2 * jp) * 128;
+                            u0[u] = ptx::ld_cg_f4(pp);
+                            u1[u] = ptx::ld_cg_f4(pp + 128);
+                        }
+                    }
+                    // Fixed rank order: y = p_0, then y = y + p_r.
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (r0 + u < a.W) {
+                            if (r0 + u == 0) {
+                                y0 = u0[u];
+                                y1 = u1[u];
+                            } else {
+                                y0.x += u0[u].x; y0.y += u0[u].y; y0.z += u0[u].z; y0.w += u0[u].w;
+                                y1.x += u1[u].x; y1.y += u1[u].y; y1.z += u1[u].z; y1.w += u1[u].w;
+                            }
+                        }
+                    }
+                }
+                const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + jp * 8;
+                if (row_ok && n < a.N) {
+                    if (a.y_fp32) {
+                        float *yp = static_cast<float *>(a.Y) + m * a.N + n;
+                        ptx::st_f4(yp, y0);
+                        ptx::st_f4(yp + 4, y1);
+                    } else {
+                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0.x, y0.y);
+                        const __nv_bfloat162 h1 = __floats2bfloat162_rn(y0.z, y0.w);
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(y1.x, y1.y);
+                        const __nv_bfloat162 h3 = __floats2bfloat162_rn(y1.z, y1.w);
+                        uint4 w;
+                        w.x = *reinterpret_cast<const uint32_t *>(&h0);
+                        w.y = *reinterpret_cast<const uint32_t *>(&h1);
+                        w.z = *reinterpret_cast<const uint32_t *>(&h2);
+                        w.w = *reinterpret_cast<const uint32_t *>(&h3);
+                        ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_empty[s]));
+        ++n_jobs;
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_rs_fused_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, const KernelArgs a)
+{
+    using Cfg = TileCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + Cfg::kStages * Cfg::kStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 4);
+        }
+        for (int s = 0; s < kRQ; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 4);
+        }
+        ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0 && a.nK > 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), Cfg::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const Sched sch{a.W, a.nM, a.nN, 7, a.R};
+
+    if (warp == 0) {
+        if (lane == 0)
+            run_producer<BN>(a, sch, &tmA, &tmB, smem, ctl);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0)
+            run_mma<BN>(a, tmem, smem, ctl);
+        __syncwarp();
+    } else if (warp < kRedWarp0) {
+        run_epilogue<BN>(a, sch, tmem, ctl, warp, lane);
+    } else {
+        run_reducer<BN>(a, ctl, warp, lane);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+} // namespace gemm_rs

@@ -1,0 +1,196 @@
+"""Parity of the fused CUDA path with the oracle, through the C ABI.
+
+Small cases are compared element by element.  They span several tiles and
+ragged tails in M, N and K, chunks that do not align with tiles, and all
+three tile widths.  The full-size workloads are compared on a row sample the
+oracle computes one row at a time.  Integer-valued inputs make every sum exact,
+so those runs must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, inputs, oracle_y, run_gpu, to_np_y
+from tensor_gemm_reduce_tcgen05_gb300.inputs import (WORKLOADS, bf16_bits, sample_rows,
+                                                     workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # W, M, N, Kpr                                      what it covers
+    (2, 256, 256, 256),    # the tiny workload: 2x1 tiles, 4 k-blocks
+    (3, 300, 520, 200),    # ragged M, N and K; chunks of 100 rows straddle tiles
+    (8, 64, 512, 192),     # 8-row chunks: one row tile holds every chunk
+    (1, 200, 72, 64),      # W = 1 is a plain GEMM; N below one tile
+    (16, 16 * 9, 136, 72), # W = 16, 9-row chunks, ragged K
+    (4, 512, 768, 128),    # several row tiles per chunk
+]
+
+
+@pytest.mark.parametrize("tile_n", [256, 128, 64])
+@pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
+def test_integer_inputs_bit_exact(W, M, N, Kpr, tile_n):
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    y, plan, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_n=tile_n)
+    assert plan["bn"] == tile_n
+    ref = oracle_y(A, B, None, 1.0, 0.0, "fp32")
+    np.testing.assert_array_equal(y, ref)
+
+
+@pytest.mark.parametrize("W,M,N,Kpr", SHAPES[:3])
+def test_integer_inputs_with_c_bit_exact(W, M, N, Kpr):
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
+    for y_dtype in ("fp32", "bf16"):
+        y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype)
+        ref = oracle_y(A, B, C, 0.5, 1.0, y_dtype)
+        np.testing.assert_array_equal(y, ref)
+
+
+@pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
+@pytest.mark.parametrize("y_dtype", ["fp32", "bf16"])
+def test_normal_inputs_within_tolerance(W, M, N, Kpr, y_dtype):
+    A, B, C = inputs(W, M, N, Kpr, "normal", c_dist="normal1")
+    y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype)
+    assert_close(y, oracle_y(A, B, C, 0.5, 1.0, y_dtype), y_dtype, f"{(W, M, N, Kpr)}")
+
+
+def test_tiny_workload_full_compare():
+    w = WORKLOADS["tiny_w2"]
+    A, B, C = workload_inputs(w)
+    y, _, _ = run_gpu(A, B, C, w.W, w.M, w.N, w.Kpr, w.alpha, w.beta, w.y_dtype)
+    assert_close(y, oracle_y(A, B, C, w.alpha, w.beta, w.y_dtype), w.y_dtype, w.name)
+
+
+def test_nan_poisoned_workspace_and_output():
+    """Every partial slot that is read is written in the same call, and every
+    output element is written."""
+    W, M, N, Kpr = 3, 300, 520, 200
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    for tile_n in (256, 64):
+        y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_n=tile_n, poison=True)
+        np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+
+
+def test_beta_zero_ignores_nan_c():
+    W, M, N, Kpr = 2, 256, 256, 64
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    from tensor_gemm_reduce_tcgen05_gb300.binding import GemmRS
+    op = GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    Cnan = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda:0")
+    Y = op.run(A.cuda(), B.cuda(), Cnan)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+
+
+def test_k_zero_gives_w_beta_c():
+    W, M, N = 4, 256, 264
+    _, _, C = inputs(W, M, N, 8, "int", c_dist="normal1")
+    A = torch.zeros((W, M, 0), dtype=torch.bfloat16)
+    B = torch.zeros((W, 0, N), dtype=torch.bfloat16)
+    y, _, _ = run_gpu(A, B, C, W, M, N, 0, 1.0, 1.0, "fp32")
+    np.testing.assert_array_equal(y, W * C.float().numpy())
+
+
+def test_empty_problem_is_a_no_op():
+    from tensor_gemm_reduce_tcgen05_gb300.binding import GemmRS
+    op = GemmRS(0, 64, 128, 2, 1.0, 0.0, "fp32", device="cuda:0")
+    A = torch.zeros((2, 0, 64), dtype=torch.bfloat16, device="cuda:0")
+    B = torch.zeros((2, 64, 64), dtype=torch.bfloat16, device="cuda:0")
+    op.run(A, B)
+    torch.cuda.synchronize()
+    assert op.status() == 0
+
+
+def test_twenty_calls_bit_identical_and_counters_reset():
+    """Workspace reused across back-to-back calls with no memset: identical
+    results every call, and every tile counter is 0 afterwards."""
+    W, M, N, Kpr = 4, 1024, 640, 256
+    A, B, _ = inputs(W, M, N, Kpr, "uniform")
+    from tensor_gemm_reduce_tcgen05_gb300.binding import GemmRS
+    op = GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    Ad, Bd = A.cuda(), B.cuda()
+    outs = [op.run(Ad, Bd) for _ in range(20)]
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    first = outs[0].cpu()
+    for o in outs[1:]:
+        assert torch.equal(o.cpu().view(torch.int32), first.view(torch.int32))
+    assert int(op.flags_view().abs().sum()) == 0
+    assert_close(first.numpy(), oracle_y(A, B, None, 1.0, 0.0, "fp32"), "fp32", "20 calls")
+
+
+def test_device_schedule_record_matches_schedule_and_oracle():
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    for (W, M, N, Kpr, tile_n) in [(8, 1024, 1024, 64, 256), (3, 300, 520, 64, 128),
+                                    (8, 64, 8192, 64, 64)]:
+        A, B, _ = inputs(W, M, N, Kpr, "int")
+        op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_n=tile_n)
+        nM, nN = -(-M // 128), -(-N // tile_n)
+        rec = torch.full((W * nM * nN, 4), -1, dtype=torch.int32, device="cuda:0")
+        b.gemm_rs_set_debug(op.handle, rec.data_ptr(), 0)
+        Y = op.run(A.cuda(), B.cuda())
+        torch.cuda.synchronize()
+        rec = rec.cpu().numpy()
+        lib_sched = b.gemm_rs_schedule(M, N, W, 128, tile_n)
+        np.testing.assert_array_equal(rec[:, :3], lib_sched)
+        np.testing.assert_array_equal(rec[:, :3], oracle.schedule(W, M, N, 128, tile_n))
+        grid = op.plan["grid"]
+        np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % grid)
+        np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+
+
+def test_timeout_path_reports_and_recovers():
+    """A stalled producer makes the MMA warp's bounded wait run out.  The
+    kernel records the timeout, exits, and the context stays usable."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 2, 256, 256, 128
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    Ad, Bd = A.cuda(), B.cuda()
+    b.gemm_rs_set_timeout_cycles(op.handle, 1 << 22)
+    b.gemm_rs_set_debug(op.handle, 0, b.GEMM_RS_DEBUG_STALL_PRODUCER)
+    op.run(Ad, Bd)
+    assert op.status() == b.GEMM_RS_ERR_TIMEOUT
+    assert "timed out" in b.gemm_rs_last_error()
+    assert op.status() == b.GEMM_RS_OK        # the status word was cleared
+    b.gemm_rs_set_debug(op.handle, 0, 0)
+    b.gemm_rs_set_timeout_cycles(op.handle, 1 << 32)
+    op.reset()
+    Y = op.run(Ad, Bd)
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+
+
+def test_baseline_reduce_kernel_matches_oracle():
+    """The unfused baseline's separate reduce step, given exact per-rank
+    partials, reproduces the oracle's fold."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 4, 256, 264, 64
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
+    P = torch.stack([A[r].float() @ B[r].float() for r in range(W)]).cuda().contiguous()
+    for y_dtype in ("fp32", "bf16"):
+        Y = torch.empty((M, N), dtype=torch.float32 if y_dtype == "fp32" else torch.bfloat16,
+                        device="cuda:0")
+        b.gemm_rs_reduce_partials(P.data_ptr(), b.GEMM_RS_FP32, C.cuda().data_ptr(), Y.data_ptr(),
+                                  M, N, W, 0.5, 1.0,
+                                  b.GEMM_RS_FP32 if y_dtype == "fp32" else b.GEMM_RS_BF16)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, C, 0.5, 1.0, y_dtype))
+
+
+@pytest.mark.parametrize("name", ["ffn_w8_m4096", "ffn_w8_m8192_bias", "decode_w8_m64",
+                                  "ffn_w4_m16384_x20"])
+def test_full_size_workloads_on_row_sample(name):
+    """The full-size workloads in the launch configuration the benchmark
+    times, checked on a row sample: every chunk's first and last row, every
+    row-tile boundary, and 64 seeded random rows."""
+    w = WORKLOADS[name]
+    A, B, C = workload_inputs(w)
+    y, plan, op = run_gpu(A, B, C, w.W, w.M, w.N, w.Kpr, w.alpha, w.beta, w.y_dtype,
+                          calls=w.calls)
+    rows = sample_rows(w.M, w.W)
+    ref = oracle_y(A, B, C, w.alpha, w.beta, w.y_dtype, rows=rows)
+    assert_close(y[rows], ref, w.y_dtype, name)
+    assert int(op.flags_view().abs().sum()) == 0
