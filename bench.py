@@ -1,0 +1,526 @@
+"""Benchmark of the fused GEMM + reduce-scatter on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole hot path: one fused-kernel call that computes
+Y = sum_r (alpha*A_r*B_r + beta*C) over one batch of synthetic inputs.  By default
+the workload is ffn_w8_m4096: W = 8 logical ranks, M = N = 4096, K = 14336
+(1792 per rank), bf16 inputs, bf16 Y.  Inputs are seeded and synthetic (see
+tensor_gemm_reduce_tcgen05_gb300/inputs.py) and stay resident in HBM during the
+timed region.  A + B (235 MB) plus the partial workspace (537 MB) are larger
+than the 129 MB L2, so no L2 flush is needed between steps.
+
+Rank 0 prints one JSON line.  It has the metric (fused TFLOP/s, whole job), the
+kernel's roofline fraction, the end-to-end figure through the public API with
+host<->device copies in the timed region, the unfused same-GPU baseline
+(batched cuBLAS per-rank GEMMs, then the library's separate reduce kernel), a
+full-K GEMM for context, the clear-kernel-sync ablation, the oracle timed on
+the host cores (cpu_baseline), and the SM clocks sampled during the run.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU.
+The path has no cross-GPU exchange here, so there are no collectives on the
+data path.  Timing is the max over ranks.
+
+--impl reference times the CPU oracle (the only reference this path has) on a
+bounded row sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+RS TFLOP/s and % of GB300 bf16 tensor peak vs unfused, 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Max of a float over all ranks (identity at world size 1)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_gemm_reduce_tcgen05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    if that summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"gemm_rs_fused_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while active."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        power = [num(r[3]) for r in loaded if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+def algorithmic_bytes(w) -> int:
+    """Compulsory bytes of one call: A + B (+ C once per rank when beta != 0) + Y,
+    plus the reduce-scatter exchange through the workspace: (W-1)*M*N fp32
+    partials written and read back."""
+    a = w.W * w.M * w.Kpr * 2
+    b = w.W * w.Kpr * w.N * 2
+    c = w.W * w.M * w.N * 2 if w.beta != 0 else 0
+    y = w.M * w.N * (2 if w.y_dtype == "bf16" else 4)
+    ex = 2 * (w.W - 1) * w.M * w.N * 4
+    return a + b + c + y + ex
+
+
+def oracle_sample(w, A, B, C, rows_wanted: int, threads: int):
+    """Time the oracle on `rows_wanted` evenly spread rows.  Returns (seconds, rows)."""
+    import oracle
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import bf16_bits
+    step = max(1, w.M // max(1, rows_wanted))
+    rows = list(range(0, w.M, step))[:rows_wanted]
+    Ab, Bb = bf16_bits(A), bf16_bits(B)
+    Cb = None if C is None else bf16_bits(C)
+    t0 = time.perf_counter()
+    oracle.gemm_rs(Ab, Bb, Cb, w.alpha, w.beta, w.y_dtype, rows=rows, threads=threads)
+    return time.perf_counter() - t0, len(rows)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def calibrate_rows(w, A, B, C, threads: int, target_s: float):
+    """Rows per oracle sample such that one sample takes about target_s seconds."""
+    t, n = oracle_sample(w, A, B, C, threads, threads)
+    per_row = t / n
+    rows = max(threads, int(target_s / per_row) // threads * threads)
+    return min(rows, w.M), per_row
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[args.workload]
+    A, B, C = workload_inputs(w)
+    cores = host_cores()
+    # Each step is a bounded row sample (about 2 s), so that warm-up + steps end
+    # within a few minutes.
+    rows, _ = calibrate_rows(w, A, B, C, cores, target_s=2.0)
+    for _ in range(args.warmup):
+        oracle_sample(w, A, B, C, rows, cores)
+    times = []
+    for _ in range(args.steps):
+        t, n = oracle_sample(w, A, B, C, rows, cores)
+        times.append(t)
+    sec = sum(times) / len(times)
+    flops = 2.0 * rows * w.N * w.K
+    value = flops / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} of {w.M} output rows per step (all N columns, all W ranks)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w) -> dict:
+    return {"workload": w.name, "W": w.W, "M": w.M, "N": w.N, "K": w.K, "K_per_rank": w.Kpr,
+            "alpha": w.alpha, "beta": w.beta, "y_dtype": w.y_dtype,
+            "inputs": f"A {w.a_dist}, B {w.b_dist}" + (f", C {w.c_dist}" if w.c_dist else ""),
+            "l2": l2_note(w)}
+
+
+def l2_note(w) -> str:
+    ab = w.W * w.M * w.Kpr * 2 + w.W * w.Kpr * w.N * 2
+    ws = w.W * w.M * w.N * 4
+    if ab + ws > L2_BYTES:
+        return (f"inputs larger than L2: A+B {ab / 1e6:.0f} MB + partial workspace {ws / 1e6:.0f} MB"
+                " > 129 MB L2, no flush between steps")
+    return (f"working set {(ab + ws) / 1e6:.1f} MB fits in L2 (latency case); "
+            "reported as time per call, not as an HBM figure")
+
+
+# --------------------------------------------------------------------------- our arm
+def time_loop(fn, steps, stream):
+    import torch
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(steps):
+        fn()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def run_ours(args):
+    import torch
+    from tensor_gemm_reduce_tcgen05_gb300 import binding
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import WORKLOADS, workload_inputs
+
+    rank, world, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    w = WORKLOADS[args.workload]
+    peaks = load_peaks()
+    binding.lib()
+
+    A, B, C = workload_inputs(w)
+    A_pin, B_pin = A.pin_memory(), B.pin_memory()
+    C_pin = None if C is None else C.pin_memory()
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = None if C is None else C.to(dev)
+    op = binding.GemmRS(w.M, w.N, w.K, w.W, w.alpha, w.beta, w.y_dtype, device=dev)
+    if args.tile_n:
+        binding.gemm_rs_set_tile_n(op.handle, args.tile_n)
+    Y = op.new_output()
+    Y_pin = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+
+    def step():
+        op.run(Ad, Bd, Cd, Y, stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout during warm-up: " + binding.gemm_rs_last_error())
+
+    # ---- timed region: K fused calls, events around each launch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    ms_step = t0.elapsed_time(t1) / args.steps
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_avg_ms = sum(kernel_ms) / len(kernel_ms)
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+
+    ms_step_max = max_over_ranks(dist, ms_step, dev)
+    value = aggregate_throughput(w.flops, world, ms_step_max / 1e3) / 1e12
+
+    if args.skip_extras:
+        clocks = sampler.stop()
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
+                "kernel_ms": kernel_avg_ms, "config": workload_config(w), "plan": op.plan,
+                "clocks": clocks, "note": "profiling run: fused kernel only"}
+        if rank == 0:
+            print(json.dumps(line))
+        op.close()
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    # ---- end to end through the public API: H2D inputs, run, D2H result
+    def e2e_step():
+        Ad.copy_(A_pin, non_blocking=True)
+        Bd.copy_(B_pin, non_blocking=True)
+        if Cd is not None:
+            Cd.copy_(C_pin, non_blocking=True)
+        op.run(Ad, Bd, Cd, Y, stream)
+        Y_pin.copy_(Y, non_blocking=True)
+
+    e2e_step()
+    barrier(dist, dev)
+    e2e_ms = max_over_ranks(dist, time_loop(e2e_step, args.steps, stream), dev)
+    h2d = A.numel() * 2 + B.numel() * 2 + (0 if C is None else C.numel() * 2)
+    d2h = Y.numel() * Y.element_size()
+    e2e_value = aggregate_throughput(w.flops, world, e2e_ms / 1e3) / 1e12
+
+    # ---- unfused same-GPU baseline: batched per-rank cuBLAS GEMMs into fp32
+    # partials, then the library's separate reduce kernel
+    P = torch.empty((w.W, w.M, w.N), dtype=torch.float32, device=dev)
+    p_dtype = binding.GEMM_RS_FP32
+    try:
+        torch.bmm(Ad, Bd, out_dtype=torch.float32, out=P)
+        torch.cuda.synchronize()
+
+        def gemms():
+            torch.bmm(Ad, Bd, out_dtype=torch.float32, out=P)
+        partials_note = "fp32 partials (torch.bmm out_dtype=float32)"
+    except (TypeError, RuntimeError):
+        P = torch.empty((w.W, w.M, w.N), dtype=torch.bfloat16, device=dev)
+        p_dtype = binding.GEMM_RS_BF16
+
+        def gemms():
+            torch.bmm(Ad, Bd, out=P)
+        partials_note = "bf16 partials (torch.bmm)"
+    y_code = binding.GEMM_RS_BF16 if w.y_dtype == "bf16" else binding.GEMM_RS_FP32
+
+    def reduce_only():
+        binding.gemm_rs_reduce_partials(P.data_ptr(), p_dtype, 0 if Cd is None else Cd.data_ptr(),
+                                        Y.data_ptr(), w.M, w.N, w.W, w.alpha, w.beta, y_code,
+                                        stream.cuda_stream)
+
+    def unfused():
+        gemms()
+        reduce_only()
+
+    for _ in range(max(3, args.warmup)):
+        unfused()
+    unfused_ms = time_loop(unfused, args.steps, stream)
+    gemms_ms = time_loop(gemms, args.steps, stream)
+    reduce_ms = time_loop(reduce_only, args.steps, stream)
+    del P
+
+    # full-K GEMM of the same shape (no reduce-scatter at all): context
+    A_full = Ad.permute(1, 0, 2).reshape(w.M, w.K).contiguous()
+    B_full = Bd.reshape(w.K, w.N)
+    for _ in range(3):
+        torch.mm(A_full, B_full)
+    fullk_ms = time_loop(lambda: torch.mm(A_full, B_full), args.steps, stream)
+    del A_full
+
+    # clear-kernel-sync ablation: counter clear + sync + kernel + sync per call
+    def kernel_sync():
+        step()
+        torch.cuda.synchronize()
+
+    def clear_kernel_sync():
+        op.reset(stream)
+        torch.cuda.synchronize()
+        step()
+        torch.cuda.synchronize()
+
+    ks_ms = time_loop(kernel_sync, args.steps, stream)
+    cks_ms = time_loop(clear_kernel_sync, args.steps, stream)
+    clocks = sampler.stop()
+
+    # ---- roofline of the fused kernel (the only kernel of the step)
+    flops_per_launch = float(w.flops)
+    bytes_per_launch = float(algorithmic_bytes(w))
+    t_tensor = flops_per_launch / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bytes_per_launch / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops_per_launch / (kernel_avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)"}
+    else:
+        achieved = bytes_per_launch / (kernel_avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy"}
+    roof["traffic"] = recorded_traffic(w.name)
+    roof["algorithmic_bytes"] = int(bytes_per_launch)
+    roof["algorithmic_flops"] = int(flops_per_launch)
+    roof["kernel_ms"] = kernel_avg_ms
+
+    # ---- CPU baseline: the oracle on a bounded row sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = host_cores()
+        rows, _ = calibrate_rows(w, A, B, C, cores, target_s=args.cpu_seconds)
+        sec, n = oracle_sample(w, A, B, C, rows, cores)
+        cpu = {"value": 2.0 * n * w.N * w.K / sec / 1e12, "unit": "TFLOP/s", "cores": cores,
+               "kind": "oracle", "seconds": sec,
+               "sample": f"{n} of {w.M} output rows (all N columns, all W ranks), evenly spaced"}
+
+    plan = op.plan
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(w),
+            "pct_of_peak": 100.0 * (flops_per_launch / (kernel_avg_ms / 1e3) / 1e12) / peaks["bf16_tflops"],
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "unfused": {"ms_per_step": unfused_ms,
+                        "value": w.flops / (unfused_ms / 1e3) / 1e12,
+                        "gemms_ms": gemms_ms, "reduce_ms": reduce_ms, "partials": partials_note,
+                        "fused_speedup": unfused_ms / ms_step},
+            "full_k_gemm": {"ms": fullk_ms, "value": w.flops / (fullk_ms / 1e3) / 1e12,
+                            "note": "torch.mm [M,K]x[K,N], no reduce-scatter (context)"},
+            "ablation": {"kernel_batched_ms": ms_step, "kernel_sync_ms": ks_ms,
+                         "clear_kernel_sync_ms": cks_ms},
+            "plan": plan,
+        }
+        print(json.dumps(line))
+    op.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ffn_w8_m4096")
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time only the fused kernel (no e2e, baselines, ablation or CPU oracle); "
+                         "used for profiling runs")
+    args = ap.parse_args(argv)
+    # At least three warm-up steps are always run; the JSON line reports the number run.
+    args.warmup = max(3, args.warmup)
+    args.steps = max(1, args.steps)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
