@@ -105,21 +105,26 @@ def bf16_bits(t: torch.Tensor):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def sample_rows(M: int, W: int, BM: int = 128, n_random: int = 64, seed: int = 7):
+def sample_rows(M: int, W: int, BM: int = 128, n_random: int = 64, seed: int = 7,
+                n_boundaries: int | None = None):
     """A row sample for full-size checks: the first and last row of every
-    chunk, every BM boundary row (and the row before it), and n_random
+    chunk, row-tile boundary rows (the first row of a tile and the row before
+    it; all boundaries, or n_boundaries evenly spaced ones), and n_random
     seeded random rows.  Returned sorted and unique."""
     R = M // W
     rows = set()
     for c in range(W):
         rows.add(c * R)
         rows.add(c * R + R - 1)
-    for b in range(0, M, BM):
+    bounds = list(range(BM, M, BM))
+    if n_boundaries is not None and len(bounds) > n_boundaries:
+        step = len(bounds) / n_boundaries
+        bounds = [bounds[int(i * step)] for i in range(n_boundaries)]
+    for b in bounds:
         rows.add(b)
-        if b > 0:
-            rows.add(b - 1)
+        rows.add(b - 1)
     g = torch.Generator().manual_seed(seed)
-    if M > 0:
+    if M > 0 and n_random > 0:
         for v in torch.randint(0, M, (n_random,), generator=g).tolist():
             rows.add(int(v))
     return sorted(r for r in rows if 0 <= r < M)
