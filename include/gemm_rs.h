@@ -224,6 +224,51 @@ GEMM_RS_API int gemm_rs_reduce_partials(const void *partials, gemm_rs_dtype part
                             void *Y, int64_t M, int64_t N, int W, float alpha, float beta,
                             gemm_rs_dtype y_dtype, gemm_rs_stream_t stream);
 
+/*
+ * Size of the static device scratch used by gemm_rs_run_noalloc: 64 MiB.  It holds
+ * the status word, the tile counters and the fp32 partial tiles, laid out as in the
+ * workspace of gemm_rs_create.  A shape fits if gemm_rs_workspace_bytes(M, N, K, W)
+ * is at most this size.
+ */
+#define GEMM_RS_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * gemm_rs_run without a handle and without a workspace: this call allocates
+ * nothing.  (The pages have no counterpart.  This is a convenience of this
+ * library.)
+ *
+ * Some callers cannot call cudaMalloc and have no workspace to hand over.
+ * Examples: a plugin inside a host application that owns every device
+ * allocation, or a latency-critical path where an allocation, which may
+ * synchronise the device, is not allowed.  This entry point runs the same fused
+ * kernel.  Its scratch (status word, tile counters, partial tiles) is a
+ * file-scope device array of GEMM_RS_NOALLOC_SCRATCH_BYTES, which every GPU that
+ * loads this library holds until the process exits.  The call makes no
+ * cudaMalloc or cudaFree and calls no allocating library routine.
+ *
+ *   M, N, K, W, alpha, beta, y_dtype   as for gemm_rs_create (A, B and C are bf16).
+ *   A, B, C, Y                         as for gemm_rs_run (device, 16-byte aligned).
+ *   stream                             the call is asynchronous on this stream.
+ *
+ * - The first call on a device does a one-time set-up on that device: kernel
+ *   attributes, plus a cudaGetSymbolAddress lookup of the scratch array.  Make
+ *   that first call before any stream capture begins.
+ * - Each call clears the status word and the tile counters with one
+ *   cudaMemsetAsync on `stream`.  The scratch keeps the previous call's
+ *   contents otherwise.
+ * - Every call on a device shares the one scratch array.  Calls that overlap
+ *   on the GPU (different streams, or host threads with no ordering between
+ *   them) race on it and give wrong results.  Order them on one stream.
+ * - A shape whose gemm_rs_workspace_bytes exceeds GEMM_RS_NOALLOC_SCRATCH_BYTES
+ *   is rejected with GEMM_RS_ERR_WORKSPACE.  Other errors are as for
+ *   gemm_rs_create and gemm_rs_run.  Device-side timeouts are not reported:
+ *   use a handle (gemm_rs_status) when that is needed.
+ */
+GEMM_RS_API int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float alpha,
+                                    float beta, gemm_rs_dtype y_dtype, const void *A,
+                                    const void *B, const void *C, void *Y,
+                                    gemm_rs_stream_t stream);
+
 /* Library version string. */
 GEMM_RS_API const char *gemm_rs_version(void);
 

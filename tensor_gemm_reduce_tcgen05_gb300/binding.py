@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_set_debug": (i32, [vp, vp, i32]),
             "gemm_rs_reduce_partials": (i32, [vp, i32, vp, vp, i64, i64, i32, f32, f32, i32, vp]),
             "gemm_rs_version": (ctypes.c_char_p, []),
+            "gemm_rs_run_noalloc": (i32, [i64, i64, i64, i32, f32, f32, i32, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -163,6 +164,15 @@ def gemm_rs_reduce_partials(partials, partial_dtype, C, Y, M, N, W, alpha, beta,
                             stream=0) -> None:
     _check(lib().gemm_rs_reduce_partials(partials, partial_dtype, C, Y, M, N, W, alpha, beta,
                                          y_dtype, stream))
+
+
+def gemm_rs_run_noalloc(M, N, K, W, alpha, beta, y_dtype, A, B, C, Y, stream=0) -> None:
+    """The handle-free entry point whose scratch is a static device array
+    (see include/gemm_rs.h): it allocates nothing."""
+    _check(lib().gemm_rs_run_noalloc(M, N, K, W, alpha, beta, y_dtype, A, B, C, Y, stream))
+
+
+GEMM_RS_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 def _stream_ptr(stream) -> int:

@@ -7,6 +7,7 @@
 #include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -515,3 +516,147 @@ int gemm_rs_reduce_partials(const void *partials, gemm_rs_dtype partial_dtype, c
 }
 
 } // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// Entry point that allocates nothing: gemm_rs_run_noalloc.
+//
+// Some callers cannot call cudaMalloc and have no workspace to hand over.  Examples: a
+// plugin inside a host application that owns every device allocation, or a
+// latency-critical path where an allocation, which may synchronise the device, is not
+// allowed.  For them, the fused kernel's scratch (status word, tile counters and fp32
+// partial tiles) lives in the file-scope array below.  Every GPU that loads this library
+// holds the array until the process exits.  The caller still passes A, B, C and Y.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(GEMM_RS_NOALLOC_SCRATCH_BYTES);
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    uint8_t *scratch = nullptr; // device address of g_noalloc_scratch on this device
+    int sms = 0;
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: kernel attributes and the device address of
+// the scratch array.  In host code the array's name is only a host-side stand-in, so
+// the address must come from cudaGetSymbolAddress.
+int noalloc_device(int *dev_out, uint8_t **scratch_out, int *sms_out)
+{
+    int dev = 0, sms = 0;
+    int rc = prepare_device(&dev, &sms);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (d.scratch == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        if (!aligned(p, 256))
+            return fail(GEMM_RS_ERR_ALIGN, "static scratch is not 256-byte aligned");
+        d.scratch = static_cast<uint8_t *>(p);
+        d.sms = sms;
+    }
+    *dev_out = dev;
+    *scratch_out = d.scratch;
+    *sms_out = d.sms;
+    return GEMM_RS_OK;
+}
+
+} // namespace
+
+extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float alpha, float beta,
+                                   gemm_rs_dtype y_dtype, const void *A, const void *B,
+                                   const void *C, void *Y, gemm_rs_stream_t stream)
+{
+    int rc = check_shape(M, N, K, W);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    if (y_dtype != GEMM_RS_BF16 && y_dtype != GEMM_RS_FP32)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "Y dtype must be GEMM_RS_BF16 or GEMM_RS_FP32");
+    if (!(alpha == alpha) || !(beta == beta))
+        return fail(GEMM_RS_ERR_ARG, "alpha and beta must not be NaN");
+    const Layout L = layout_for(M, N, W);
+    if (L.total > kNoAllocScratchBytes)
+        return fail(GEMM_RS_ERR_WORKSPACE,
+                    "this shape needs %zu bytes of scratch; the static scratch of "
+                    "gemm_rs_run_noalloc holds %zu (use gemm_rs_create with a workspace)",
+                    L.total, kNoAllocScratchBytes);
+    if (M == 0 || N == 0)
+        return GEMM_RS_OK;
+    if (Y == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "Y is NULL");
+    if (!aligned(Y, 16))
+        return fail(GEMM_RS_ERR_ALIGN, "Y must be 16-byte aligned");
+    if (beta != 0.0f && (C == nullptr || !aligned(C, 16)))
+        return fail(C == nullptr ? GEMM_RS_ERR_ARG : GEMM_RS_ERR_ALIGN,
+                    "C must be non-NULL and 16-byte aligned when beta != 0");
+    const int64_t Kpr = K / W;
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (Kpr > 0) {
+        if (A == nullptr || B == nullptr)
+            return fail(GEMM_RS_ERR_ARG, "A or B is NULL");
+        if (!aligned(A, 16) || !aligned(B, 16))
+            return fail(GEMM_RS_ERR_ALIGN, "A and B must be 16-byte aligned");
+        if ((rc = encode_3d(&tmA, A, Kpr, M, W, gemm_rs::kBK, gemm_rs::kBM)) != GEMM_RS_OK)
+            return rc;
+        if ((rc = encode_3d(&tmB, B, N, Kpr, W, 64, gemm_rs::kBK)) != GEMM_RS_OK)
+            return rc;
+    }
+    int dev = 0, sms = 0;
+    uint8_t *scratch = nullptr;
+    if ((rc = noalloc_device(&dev, &scratch, &sms)) != GEMM_RS_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents: the status word and the tile
+    // counters must start at zero.  The partial slots need no clearing, because every
+    // slot a call reads is written earlier in the same call.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, L.part_off, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
+
+    const int bn = pick_bn(M, N, W, sms);
+    gemm_rs::KernelArgs a;
+    a.W = W;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.nM = static_cast<int>(cdiv(M, gemm_rs::kBM));
+    a.nN = static_cast<int>(cdiv(N, bn));
+    a.nK = static_cast<int>(cdiv(Kpr, gemm_rs::kBK));
+    a.R = M / W;
+    a.total = static_cast<int64_t>(W) * a.nM * a.nN;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = beta != 0.0f ? static_cast<const uint16_t *>(C) : nullptr;
+    a.Y = Y;
+    a.y_fp32 = y_dtype == GEMM_RS_FP32 ? 1 : 0;
+    a.part = reinterpret_cast<float *>(scratch + L.part_off);
+    a.flags = reinterpret_cast<uint32_t *>(scratch + L.flags_off);
+    a.status = reinterpret_cast<uint32_t *>(scratch);
+    a.record = nullptr;
+    a.timeout = 1ull << 32;
+    a.stall_producer = 0;
+    const int grid = static_cast<int>(a.total < sms ? a.total : sms);
+    switch (bn) {
+    case 256:
+        gemm_rs::gemm_rs_fused_kernel<256>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<256>(), s>>>(tmA, tmB, a);
+        break;
+    case 128:
+        gemm_rs::gemm_rs_fused_kernel<128>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<128>(), s>>>(tmA, tmB, a);
+        break;
+    default:
+        gemm_rs::gemm_rs_fused_kernel<64>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<64>(), s>>>(tmA, tmB, a);
+        break;
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the fused GEMM+RS kernel (no-alloc entry point)");
+    return GEMM_RS_OK;
+}
