@@ -192,13 +192,20 @@ GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn
  */
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid);
 
-/* Override the tile width (bn = 256, 128 or 64).  The default is picked so
- * that there are at least four work items per SM.  Returns ERR_ARG for any
- * other value. */
+/* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
+ * (bm = 128).  Returns ERR_ARG for any other value. */
 GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
 
 /* Device wait limit in SM clock cycles (default 2^32, about two seconds).  A
  * wait that runs past it sets the status word and lets the kernel exit. */
+/* Override the output tile.  (128, 64|128|256) runs the single-CTA kernel.
+ * (256, 256) runs the CTA-pair kernel: a cluster of two CTAs shares one 256x256
+ * tile.  Each CTA loads its own 128 rows of A and 128 columns of B, and one
+ * tcgen05.mma.cta_group::2 computes the pair's product.  The default is the pair
+ * kernel when there are at least four 256x256 rank-tiles per SM pair, otherwise
+ * the widest single-CTA tile with at least four work items per SM. */
+GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
+
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
 
 /*

@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_get_plan": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                        ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "gemm_rs_set_tile_n": (i32, [vp, i32]),
+            "gemm_rs_set_tile": (i32, [vp, i32, i32]),
             "gemm_rs_set_timeout_cycles": (i32, [vp, u64]),
             "gemm_rs_set_debug": (i32, [vp, vp, i32]),
             "gemm_rs_reduce_partials": (i32, [vp, i32, vp, vp, i64, i64, i32, f32, f32, i32, vp]),
@@ -152,6 +153,10 @@ def gemm_rs_set_tile_n(h, bn: int) -> None:
     _check(lib().gemm_rs_set_tile_n(h, bn))
 
 
+def gemm_rs_set_tile(h, bm: int, bn: int) -> None:
+    _check(lib().gemm_rs_set_tile(h, bm, bn))
+
+
 def gemm_rs_set_timeout_cycles(h, cycles: int) -> None:
     _check(lib().gemm_rs_set_timeout_cycles(h, cycles))
 
@@ -191,7 +196,8 @@ class GemmRS:
     """
 
     def __init__(self, M: int, N: int, K: int, W: int, alpha: float = 1.0, beta: float = 0.0,
-                 y_dtype: str = "bf16", device=None, stream=None, tile_n: int | None = None):
+                 y_dtype: str = "bf16", device=None, stream=None, tile_n: int | None = None,
+                 tile_m: int | None = None):
         import torch
         lib()
         self.M, self.N, self.K, self.W = M, N, K, W
@@ -206,7 +212,9 @@ class GemmRS:
             self.handle = gemm_rs_create(M, N, K, W, alpha, beta, GEMM_RS_BF16, GEMM_RS_BF16,
                                          _DTYPES[y_dtype], self.workspace.data_ptr(), nbytes,
                                          _stream_ptr(stream))
-        if tile_n is not None:
+        if tile_m is not None:
+            gemm_rs_set_tile(self.handle, tile_m, tile_n if tile_n is not None else 256)
+        elif tile_n is not None:
             gemm_rs_set_tile_n(self.handle, tile_n)
 
     @property

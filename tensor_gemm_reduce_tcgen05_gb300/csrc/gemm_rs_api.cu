@@ -128,6 +128,7 @@ int encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1, uint6
 
 struct DeviceInfo {
     int sms = 0;
+    int pair_clusters = 0; // CTA pairs of the pair kernel that fit on the device at once
     bool attrs_set = false;
 };
 constexpr int kMaxDevices = 64;
@@ -141,7 +142,14 @@ cudaError_t set_kernel_attrs()
                                 gemm_rs::smem_bytes<BN>());
 }
 
-int prepare_device(int *dev_out, int *sms_out)
+cudaError_t set_pair_kernel_attrs()
+{
+    return cudaFuncSetAttribute(gemm_rs::gemm_rs_pair_kernel<256>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemm_rs::smem_bytes_pair<256>());
+}
+
+int prepare_device(int *dev_out, int *sms_out, int *pair_clusters_out = nullptr)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -164,17 +172,30 @@ int prepare_device(int *dev_out, int *sms_out)
             return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
         if ((e = set_kernel_attrs<256>()) != cudaSuccess ||
             (e = set_kernel_attrs<128>()) != cudaSuccess ||
-            (e = set_kernel_attrs<64>()) != cudaSuccess)
+            (e = set_kernel_attrs<64>()) != cudaSuccess || (e = set_pair_kernel_attrs()) != cudaSuccess)
             return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
+        cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = gemm_rs::smem_bytes_pair<256>();
+        int clusters = 0;
+        if ((e = cudaOccupancyMaxActiveClusters(&clusters, gemm_rs::gemm_rs_pair_kernel<256>, &cfg)) !=
+            cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveClusters(pair kernel)");
+        d.pair_clusters = clusters > 0 ? clusters : 1;
         d.attrs_set = true;
     }
     *dev_out = dev;
     *sms_out = d.sms;
+    if (pair_clusters_out)
+        *pair_clusters_out = d.pair_clusters;
     return GEMM_RS_OK;
 }
 
-int stages_for(int bn)
+int stages_for(int bm, int bn)
 {
+    if (bm == 2 * gemm_rs::kBM)
+        return gemm_rs::PairCfg<256>::kStages;
     switch (bn) {
     case 256: return gemm_rs::TileCfg<256>::kStages;
     case 128: return gemm_rs::TileCfg<128>::kStages;
@@ -193,6 +214,21 @@ int pick_bn(int64_t M, int64_t N, int W, int sms)
     return 64;
 }
 
+// Launch plan: the CTA-pair kernel (256 x 256 tiles) when there are at least
+// four pair tiles per SM pair, otherwise the single-CTA kernel with the widest
+// tile that still gives at least four work items per SM.
+void pick_tile(int64_t M, int64_t N, int W, int sms, int *bm, int *bn)
+{
+    const int64_t pairs = static_cast<int64_t>(W) * cdiv(M, 2 * gemm_rs::kBM) * cdiv(N, 256);
+    if (M > gemm_rs::kBM && pairs >= 4LL * (sms / 2)) {
+        *bm = 2 * gemm_rs::kBM;
+        *bn = 256;
+        return;
+    }
+    *bm = gemm_rs::kBM;
+    *bn = pick_bn(M, N, W, sms);
+}
+
 } // namespace
 
 struct gemm_rs_s {
@@ -202,7 +238,7 @@ struct gemm_rs_s {
     gemm_rs_dtype y_dtype;
     uint8_t *ws;
     Layout L;
-    int device, sms, bn;
+    int device, sms, pair_clusters, bm, bn;
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
     unsigned long long timeout;
@@ -249,8 +285,8 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     if (workspace_bytes < L.total)
         return fail(GEMM_RS_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes,
                     L.total);
-    int dev = 0, sms = 0;
-    if ((rc = prepare_device(&dev, &sms)) != GEMM_RS_OK)
+    int dev = 0, sms = 0, pair_clusters = 0;
+    if ((rc = prepare_device(&dev, &sms, &pair_clusters)) != GEMM_RS_OK)
         return rc;
     cudaError_t e = cudaMemsetAsync(workspace, 0, L.part_off, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
@@ -270,7 +306,8 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->L = L;
     h->device = dev;
     h->sms = sms;
-    h->bn = pick_bn(M, N, W, sms);
+    h->pair_clusters = pair_clusters;
+    pick_tile(M, N, W, sms, &h->bm, &h->bn);
     h->tmA_ptr = h->tmB_ptr = nullptr;
     h->timeout = 1ull << 32;
     h->record = nullptr;
@@ -289,15 +326,21 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
-    const int64_t total = static_cast<int64_t>(h->W) * cdiv(h->M, gemm_rs::kBM) * cdiv(h->N, h->bn);
+    const int64_t total = static_cast<int64_t>(h->W) * cdiv(h->M, h->bm) * cdiv(h->N, h->bn);
     if (bm)
-        *bm = gemm_rs::kBM;
+        *bm = h->bm;
     if (bn)
         *bn = h->bn;
     if (stages)
-        *stages = stages_for(h->bn);
-    if (grid)
-        *grid = static_cast<int>(total < h->sms ? total : h->sms);
+        *stages = stages_for(h->bm, h->bn);
+    if (grid) {
+        if (h->bm == 2 * gemm_rs::kBM) {
+            const int64_t pairs = h->pair_clusters;
+            *grid = static_cast<int>(2 * (total < pairs ? total : pairs));
+        } else {
+            *grid = static_cast<int>(total < h->sms ? total : h->sms);
+        }
+    }
     return GEMM_RS_OK;
 }
 
@@ -307,6 +350,20 @@ int gemm_rs_set_tile_n(gemm_rs_t h, int bn)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
     if (bn != 64 && bn != 128 && bn != 256)
         return fail(GEMM_RS_ERR_ARG, "tile width %d is not 64, 128 or 256", bn);
+    h->bm = gemm_rs::kBM;
+    h->bn = bn;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    const bool single = bm == gemm_rs::kBM && (bn == 64 || bn == 128 || bn == 256);
+    const bool pair = bm == 2 * gemm_rs::kBM && bn == 256;
+    if (!single && !pair)
+        return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not 128x{64,128,256} or 256x256", bm, bn);
+    h->bm = bm;
     h->bn = bn;
     return GEMM_RS_OK;
 }
@@ -385,8 +442,9 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nM = static_cast<int>(cdiv(h->M, gemm_rs::kBM));
     a.nN = static_cast<int>(cdiv(h->N, h->bn));
     a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
+    a.nMs = static_cast<int>(cdiv(h->M, h->bm));
     a.R = h->M / h->W;
-    a.total = static_cast<int64_t>(h->W) * a.nM * a.nN;
+    a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
     a.beta = h->beta;
     a.C = h->beta != 0.0f ? static_cast<const uint16_t *>(C) : nullptr;
@@ -399,8 +457,18 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.timeout = h->timeout;
     a.stall_producer = (h->debug_flags & GEMM_RS_DEBUG_STALL_PRODUCER) ? 1 : 0;
 
-    const int grid = static_cast<int>(a.total < h->sms ? a.total : h->sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h->bm == 2 * gemm_rs::kBM) {
+        const int64_t pairs = h->pair_clusters;
+        const int grid = static_cast<int>(2 * (a.total < pairs ? a.total : pairs));
+        gemm_rs::gemm_rs_pair_kernel<256>
+            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes_pair<256>(), s>>>(h->tmA, h->tmB, a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return cuda_fail(e, "launch of the fused GEMM+RS pair kernel");
+        return GEMM_RS_OK;
+    }
+    const int grid = static_cast<int>(a.total < h->sms ? a.total : h->sms);
     switch (h->bn) {
     case 256:
         gemm_rs::gemm_rs_fused_kernel<256>
@@ -460,11 +528,12 @@ int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *o
         return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
     if (M < 1 || N < 1 || M % W != 0)
         return fail(GEMM_RS_ERR_SHAPE, "need M, N >= 1 and M %% W == 0");
-    if (bm != gemm_rs::kBM || (bn != 64 && bn != 128 && bn != 256))
+    if ((bm != gemm_rs::kBM && bm != 2 * gemm_rs::kBM) || (bn != 64 && bn != 128 && bn != 256))
         return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not a tile of this library", bm, bn);
     if (out == nullptr)
         return fail(GEMM_RS_ERR_ARG, "out is NULL");
-    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), static_cast<int>(cdiv(N, bn)), 7, M / W};
+    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), static_cast<int>(cdiv(N, bn)),
+                           bm == gemm_rs::kBM ? 7 : 8, M / W};
     const int64_t total = static_cast<int64_t>(W) * s.nM * s.nN;
     if (cap < total)
         return fail(GEMM_RS_ERR_SHAPE, "cap %lld < %lld entries", (long long)cap, (long long)total);
@@ -627,6 +696,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.nM = static_cast<int>(cdiv(M, gemm_rs::kBM));
     a.nN = static_cast<int>(cdiv(N, bn));
     a.nK = static_cast<int>(cdiv(Kpr, gemm_rs::kBK));
+    a.nMs = a.nM;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

@@ -84,8 +84,24 @@ struct TileCfg {
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
+// CTA-pair variant: a 256 x BN output tile per cluster of two CTAs.  Each CTA
+// loads its own 128 rows of A and its own BN/2 columns of B (no multicast),
+// and the even CTA issues tcgen05.mma.cta_group::2 with M = 256.
+template <int BN>
+struct PairCfg {
+    static_assert(BN == 256, "the pair kernel uses 256-column tiles");
+    static constexpr int kABytes = kBM * kBK * 2;            // own 128 rows
+    static constexpr int kBBytes = (BN / 2) * kBK * 2;       // own BN/2 columns
+    static constexpr int kStageBytes = kABytes + kBBytes;    // 32 KB
+    static constexpr int kStages = 6;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(2 * kBM, BN, false, true);
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
 struct KernelArgs {
     int W, M, N, nM, nN, nK;
+    int nMs;        // row tiles of the schedule (nM, or ceil(M/256) for CTA pairs)
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -117,6 +133,12 @@ template <int BN>
 constexpr int smem_bytes()
 {
     return 1024 + TileCfg<BN>::kStages * TileCfg<BN>::kStageBytes + int(sizeof(SmemCtl));
+}
+
+template <int BN>
+constexpr int smem_bytes_pair()
+{
+    return 1024 + PairCfg<BN>::kStages * PairCfg<BN>::kStageBytes + int(sizeof(SmemCtl));
 }
 
 __device__ __forceinline__ void report(const KernelArgs &a, SmemCtl *ctl, uint32_t code)
@@ -265,9 +287,13 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // ------------------------------------------------------------------ epilogue
-template <int BN>
+// PAIR: the CTA is half `crank` of a 256-row pair tile.  It drains its own
+// TMEM, waits with cluster-scope acquire, and hands the accumulator back to
+// the pair's MMA thread (in CTA 0).
+template <int BN, bool PAIR>
 __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &sch, uint32_t tmem,
-                                             SmemCtl *ctl, int warp, int lane)
+                                             SmemCtl *ctl, int warp, int lane, int64_t g0,
+                                             int64_t gstride, uint32_t crank)
 {
     using Cfg = TileCfg<BN>;
     const volatile int *abort_flag = &ctl->abort;
@@ -277,18 +303,32 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     bool ok = true;
     uint32_t rq_n = 0;
     int it = 0;
-    for (int64_t g = blockIdx.x; g < a.total; g += gridDim.x, ++it) {
-        int r, mt, nt;
-        decode_tile(sch, g, r, mt, nt);
+    for (int64_t g = g0; g < a.total; g += gstride, ++it) {
+        int r, mts, nt;
+        decode_tile(sch, g, r, mts, nt);
+        const int mt = PAIR ? 2 * mts + static_cast<int>(crank) : mts;
+        const bool half_ok = mt < a.nM; // a pair's second half may lie wholly below M
         const int buf = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
-        const bool waited =
-            ptx::mbar_wait(ptx::smem_u32(&ctl->acc_full[buf]), aph, a.timeout, abort_flag);
+        const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
+        const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
+                                 : ptx::mbar_wait(fb, aph, a.timeout, abort_flag);
         if (ptx::named_bar_or(kBarEpi, 128, !(waited && ok))) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
+        if (!half_ok) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->acc_empty[buf]), 0));
+                else
+                    ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty[buf]));
+            }
+            continue;
+        }
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
@@ -306,11 +346,15 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     v[i] = 0u;
             }
             if (slab == Cfg::kSlabs - 1) {
-                // The accumulator is fully read: hand it back to the MMA warp.
+                // The accumulator is fully read: hand it back to the MMA thread.
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty[buf]));
+                if (lane == 0) {
+                    if (PAIR)
+                        ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->acc_empty[buf]), 0));
+                    else
+                        ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty[buf]));
+                }
             }
             float p[32];
 #pragma unroll
@@ -510,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const Sched sch{a.W, a.nM, a.nN, 7, a.R};
+    const Sched sch{a.W, a.nMs, a.nN, 7, a.R};
 
     if (warp == 0) {
         if (lane == 0)
@@ -521,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             run_mma<BN>(a, tmem, smem, ctl);
         __syncwarp();
     } else if (warp < kRedWarp0) {
-        run_epilogue<BN>(a, sch, tmem, ctl, warp, lane);
+        run_epilogue<BN, false>(a, sch, tmem, ctl, warp, lane, blockIdx.x, gridDim.x, 0u);
     } else {
         run_reducer<BN>(a, ctl, warp, lane);
     }
@@ -531,6 +575,231 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+// Producer of one CTA of a pair.  Both CTAs load into their own shared memory.
+// The loads count their bytes on the even CTA's `full` barrier, which only the
+// even CTA arms (expect_tx of both CTAs' bytes).
+template <int BN>
+__device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sched &sch,
+                                                  const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                                  uint8_t *smem, SmemCtl *ctl, uint32_t crank)
+{
+    using Cfg = PairCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    const uint64_t pol = ptx::policy_evict_normal();
+    const int64_t ncl = gridDim.x / 2;
+    const int64_t cid = blockIdx.x / 2;
+    uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    if (!a.stall_producer) {
+        for (int64_t g = cid; g < a.total && ok; g += ncl) {
+            int r, mt2, nt;
+            decode_tile(sch, g, r, mt2, nt);
+            if (a.record != nullptr && crank == 0) {
+                int32_t *rec = a.record + 4 * g;
+                rec[0] = r;
+                rec[1] = mt2;
+                rec[2] = nt;
+                rec[3] = static_cast<int32_t>(cid);
+            }
+            for (int kb = 0; kb < a.nK; ++kb) {
+                if (!ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,
+                                            abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = ptx::smem_u32(&ctl->full[stage]);
+                if (crank == 0)
+                    ptx::mbar_arrive_expect_tx(fb, 2 * Cfg::kStageBytes);
+                const uint32_t fb_leader = ptx::mapa(fb, 0);
+                const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
+                ptx::tma_load_3d_pair(sa, tmA, fb_leader, kb * kBK, mt2 * (2 * kBM) + crank * kBM, r,
+                                      pol);
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+                    ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
+                                          nt * BN + crank * (BN / 2) + j * 64, kb * kBK, r, pol);
+                ++issued;
+                if (++stage == Cfg::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (ok) {
+        // Tail: every stage released by the pair's MMA, so that every arrival
+        // on this CTA's barriers has landed before the CTA exits.
+        for (int i = 0; i < Cfg::kStages; ++i) {
+            if (!ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,
+                                        abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        report(a, ctl, kStatusTimeoutProducer);
+        if (crank == 0) {
+            // The even CTA's `full` barriers count both CTAs' bytes.
+            const int64_t n = issued < Cfg::kStages ? issued : Cfg::kStages;
+            for (int64_t i = 1; i <= n; ++i) {
+                const int64_t pos = issued - i;
+                const uint32_t s = static_cast<uint32_t>(pos % Cfg::kStages);
+                const uint32_t ph = static_cast<uint32_t>((pos / Cfg::kStages) & 1);
+                ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->full[s]), ph, a.timeout, nullptr);
+            }
+        } else {
+            // The odd CTA cannot observe its loads on the even CTA's barrier:
+            // give any load still in flight time to land (2^20 cycles) before
+            // the CTA pair tears down.
+            const unsigned long long t0 = clock64();
+            while (clock64() - t0 < (1ull << 20)) {
+            }
+        }
+    }
+}
+
+// MMA issuer of the pair (one thread of the even CTA).
+template <int BN>
+__device__ __forceinline__ void run_mma_pair(const KernelArgs &a, uint32_t tmem, uint8_t *smem,
+                                             SmemCtl *ctl)
+{
+    using Cfg = PairCfg<BN>;
+    const volatile int *abort_flag = &ctl->abort;
+    const int64_t ncl = gridDim.x / 2;
+    const int64_t cid = blockIdx.x / 2;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int it = 0;
+    for (int64_t g = cid; g < a.total; g += ncl, ++it) {
+        const int buf = it & 1;
+        const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+        if (!ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->acc_empty[buf]), aph ^ 1u, a.timeout,
+                                    abort_flag)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < a.nK; ++kb) {
+            if (!ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->full[stage]), phase, a.timeout,
+                                        abort_flag)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
+            const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                // Same descriptors as the single-CTA kernel: they describe this
+                // CTA's 128 rows of A and BN/2 columns of B.  The peer CTA holds
+                // its halves at the same offsets.
+                const uint64_t ad = ptx::sdesc_sw128(sa + kk * 32, 0, 1024);
+                const uint64_t bd = ptx::sdesc_sw128(sb + kk * 2048, 8192, 1024);
+                ptx::mma_bf16_ss_pair(d, ad, bd, Cfg::kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            const uint32_t eb = ptx::smem_u32(&ctl->empty[stage]);
+            ptx::mma_commit_pair(ptx::mapa(eb, 0));
+            ptx::mma_commit_pair(ptx::mapa(eb, 1));
+            if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok)
+            break;
+        const uint32_t ab = ptx::smem_u32(&ctl->acc_full[buf]);
+        if (a.nK > 0) {
+            ptx::mma_commit_pair(ptx::mapa(ab, 0));
+            ptx::mma_commit_pair(ptx::mapa(ab, 1));
+        } else {
+            ptx::mbar_arrive_cluster(ptx::mapa(ab, 0));
+            ptx::mbar_arrive_cluster(ptx::mapa(ab, 1));
+        }
+    }
+    if (!ok) {
+        report(a, ctl, kStatusTimeoutMma);
+        ptx::mma_commit_pair(ptx::mapa(ptx::smem_u32(&ctl->drain), 0));
+        ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->drain), 0u, a.timeout, nullptr);
+    }
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_rs_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const KernelArgs a)
+{
+    using Cfg = PairCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + Cfg::kStages * Cfg::kStageBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t crank = ptx::cluster_ctarank();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 8); // 4 epilogue warps x 2 CTAs
+        }
+        for (int s = 0; s < kRQ; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 4);
+        }
+        ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0 && a.nK > 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(&ctl->tmem_base), Cfg::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync(); // the peer's barriers are initialised before any remote arrival
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const Sched sch{a.W, a.nMs, a.nN, 8, a.R};
+
+    if (warp == 0) {
+        if (lane == 0)
+            run_producer_pair<BN>(a, sch, &tmA, &tmB, smem, ctl, crank);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && crank == 0)
+            run_mma_pair<BN>(a, tmem, smem, ctl);
+        __syncwarp();
+    } else if (warp < kRedWarp0) {
+        run_epilogue<BN, true>(a, sch, tmem, ctl, warp, lane, blockIdx.x / 2, gridDim.x / 2, crank);
+    } else {
+        run_reducer<BN>(a, ctl, warp, lane);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync(); // no CTA leaves while its peer may still signal it
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem, Cfg::kTmemCols);
     }
 }
 

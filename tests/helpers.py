@@ -49,11 +49,13 @@ def assert_close(y_gpu: np.ndarray, y_ref: np.ndarray, y_dtype: str, what: str =
     assert np.all(np.isfinite(g)) == np.all(np.isfinite(r)), f"{what}: non-finite mismatch"
 
 
-def run_gpu(A, B, C, W, M, N, Kpr, alpha, beta, y_dtype, tile_n=None, calls=1, poison=False):
+def run_gpu(A, B, C, W, M, N, Kpr, alpha, beta, y_dtype, tile_n=None, calls=1, poison=False,
+            tile_m=None):
     """Run the fused path through the C ABI.  Returns (Y as numpy, plan, op)."""
     from tensor_gemm_reduce_tcgen05_gb300.binding import GemmRS
     dev = torch.device("cuda", 0)
-    op = GemmRS(M, N, W * Kpr, W, alpha, beta, y_dtype, device=dev, tile_n=tile_n)
+    op = GemmRS(M, N, W * Kpr, W, alpha, beta, y_dtype, device=dev, tile_n=tile_n,
+                tile_m=tile_m)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = None if C is None else C.to(dev)
     Y = op.new_output()

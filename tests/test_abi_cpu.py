@@ -54,6 +54,9 @@ def test_schedule_matches_oracle(b, W, M, N, bn):
     ours = b.gemm_rs_schedule(M, N, W, 128, bn)
     ref = oracle.schedule(W, M, N, 128, bn)
     np.testing.assert_array_equal(ours, ref)
+    # the CTA-pair kernel walks 256-row tiles
+    np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256),
+                                  oracle.schedule(W, M, N, 256, 256))
 
 
 def test_workspace_bytes(b):

@@ -28,21 +28,27 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("tile_n", [256, 128, 64])
+TILES = [(128, 256), (128, 128), (128, 64), (256, 256)]  # (256, 256): the CTA-pair kernel
+
+
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
-def test_integer_inputs_bit_exact(W, M, N, Kpr, tile_n):
+def test_integer_inputs_bit_exact(W, M, N, Kpr, tile):
     A, B, _ = inputs(W, M, N, Kpr, "int")
-    y, plan, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_n=tile_n)
-    assert plan["bn"] == tile_n
+    y, plan, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
+                         tile_n=tile[1])
+    assert (plan["bm"], plan["bn"]) == tile
     ref = oracle_y(A, B, None, 1.0, 0.0, "fp32")
     np.testing.assert_array_equal(y, ref)
 
 
+@pytest.mark.parametrize("tile", [(128, 256), (256, 256)])
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES[:3])
-def test_integer_inputs_with_c_bit_exact(W, M, N, Kpr):
+def test_integer_inputs_with_c_bit_exact(W, M, N, Kpr, tile):
     A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
     for y_dtype in ("fp32", "bf16"):
-        y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype)
+        y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype, tile_m=tile[0],
+                          tile_n=tile[1])
         ref = oracle_y(A, B, C, 0.5, 1.0, y_dtype)
         np.testing.assert_array_equal(y, ref)
 
@@ -67,8 +73,9 @@ def test_nan_poisoned_workspace_and_output():
     output element is written."""
     W, M, N, Kpr = 3, 300, 520, 200
     A, B, _ = inputs(W, M, N, Kpr, "int")
-    for tile_n in (256, 64):
-        y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_n=tile_n, poison=True)
+    for tile in ((128, 256), (128, 64), (256, 256)):
+        y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
+                          tile_n=tile[1], poison=True)
         np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
@@ -122,31 +129,35 @@ def test_twenty_calls_bit_identical_and_counters_reset():
 
 def test_device_schedule_record_matches_schedule_and_oracle():
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
-    for (W, M, N, Kpr, tile_n) in [(8, 1024, 1024, 64, 256), (3, 300, 520, 64, 128),
-                                    (8, 64, 8192, 64, 64)]:
+    for (W, M, N, Kpr, bm, bn) in [(8, 1024, 1024, 64, 128, 256), (3, 300, 520, 64, 128, 128),
+                                   (8, 64, 8192, 64, 128, 64), (8, 4096, 1024, 64, 256, 256),
+                                   (3, 300, 520, 64, 256, 256)]:
         A, B, _ = inputs(W, M, N, Kpr, "int")
-        op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_n=tile_n)
-        nM, nN = -(-M // 128), -(-N // tile_n)
+        op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_m=bm, tile_n=bn)
+        nM, nN = -(-M // bm), -(-N // bn)
         rec = torch.full((W * nM * nN, 4), -1, dtype=torch.int32, device="cuda:0")
         b.gemm_rs_set_debug(op.handle, rec.data_ptr(), 0)
         Y = op.run(A.cuda(), B.cuda())
         torch.cuda.synchronize()
         rec = rec.cpu().numpy()
-        lib_sched = b.gemm_rs_schedule(M, N, W, 128, tile_n)
+        lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn)
         np.testing.assert_array_equal(rec[:, :3], lib_sched)
-        np.testing.assert_array_equal(rec[:, :3], oracle.schedule(W, M, N, 128, tile_n))
+        np.testing.assert_array_equal(rec[:, :3], oracle.schedule(W, M, N, bm, bn))
         grid = op.plan["grid"]
-        np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % grid)
+        workers = grid // 2 if bm == 256 else grid  # CTA pairs process one entry each
+        np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % workers)
         np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
-def test_timeout_path_reports_and_recovers():
+@pytest.mark.parametrize("tile", [(128, 256), (256, 256)])
+def test_timeout_path_reports_and_recovers(tile):
     """A stalled producer makes the MMA warp's bounded wait run out.  The
     kernel records the timeout, exits, and the context stays usable."""
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
-    W, M, N, Kpr = 2, 256, 256, 128
+    W, M, N, Kpr = 2, 512, 256, 128
     A, B, _ = inputs(W, M, N, Kpr, "int")
-    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_m=tile[0],
+                  tile_n=tile[1])
     Ad, Bd = A.cuda(), B.cuda()
     b.gemm_rs_set_timeout_cycles(op.handle, 1 << 22)
     b.gemm_rs_set_debug(op.handle, 0, b.GEMM_RS_DEBUG_STALL_PRODUCER)
