@@ -56,7 +56,9 @@ constexpr int kBK = 64;
 constexpr int kThreads = 320;
 constexpr int kEpiWarp0 = 2;
 constexpr int kRedWarp0 = 6;
-constexpr int kRQ = 16;          // depth of the reduce queue
+constexpr int kRQ = 32;          // depth of the reduce queue (entries are quarter-tiles)
+constexpr int kConsumers = 8;    // warps that take reduce jobs: 4 reducers + 4 epilogue warps
+static_assert(kRQ >= 2 * kConsumers, "queue slots must outnumber consumers (parity reuse)");
 constexpr uint32_t kBarEpi = 1;  // named barrier of the 128 epilogue threads
 constexpr int kMaxStages = 8;
 
@@ -125,6 +127,7 @@ struct SmemCtl {
     uint64_t rq_empty[kRQ];
     uint64_t drain;
     int32_t rq_tile[kRQ];
+    uint32_t rq_head; // next queue entry to claim
     uint32_t tmem_base;
     int abort;
 };
@@ -286,6 +289,142 @@ __device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// ------------------------------------------------------------------ reduce queue
+// Single producer (epilogue thread 0), several consumer warps.  An entry is
+// (tile << 2) | quarter, or -1 to stop one consumer.  Consumers claim entries
+// in order through ctl->rq_head.  An entry's slot is released as soon as it is
+// read.
+__device__ __forceinline__ bool rq_push(const KernelArgs &a, SmemCtl *ctl, uint32_t &rq_n,
+                                        int32_t entry)
+{
+    const uint32_t s = rq_n % kRQ;
+    const uint32_t ph = (rq_n / kRQ) & 1u;
+    if (!ptx::mbar_wait(ptx::smem_u32(&ctl->rq_empty[s]), ph ^ 1u, a.timeout, &ctl->abort))
+        return false;
+    ctl->rq_tile[s] = entry;
+    ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_full[s]));
+    ++rq_n;
+    return true;
+}
+
+// One warp reduces one quarter (32 rows x BN columns) of an output tile: the
+// W partials are folded in rank order, converted, and written to Y.
+template <int BN>
+__device__ __forceinline__ void reduce_quarter(const KernelArgs &a, int tile, int q, int lane)
+{
+    using Cfg = TileCfg<BN>;
+    constexpr int S = Cfg::kSlabs;
+    const int mt = tile / a.nN;
+    const int nt = tile - mt * a.nN;
+    const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+    const bool row_ok = m < a.M;
+    // rank 0's 32-row quarter; rank r's is kSlotFloats further on
+    const float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
+                      static_cast<int64_t>(q) * S * 1024;
+    // Lane r < W prefetches rank r's 4 KB block of a slab into L2, two slabs
+    // ahead of the loads.
+    const bool pf_lane = lane < a.W;
+    const float *pf_base = qb + static_cast<int64_t>(pf_lane ? lane : 0) * Cfg::kSlotFloats;
+    if (pf_lane) {
+        ptx::bulk_prefetch_l2(pf_base, 4096);
+        if (S > 1)
+            ptx::bulk_prefetch_l2(pf_base + 1024, 4096);
+    }
+#pragma unroll 1
+    for (int slab = 0; slab < S; ++slab) {
+        if (pf_lane && slab + 2 < S)
+            ptx::bulk_prefetch_l2(pf_base + (slab + 2) * 1024, 4096);
+        const float *sb = qb + slab * 1024 + lane * 4;
+#pragma unroll 1
+        for (int jq = 0; jq < 4; ++jq) {
+            // float4 j = 2*jq and 2*jq+1: columns 8*jq .. 8*jq+7 of the slab.
+            float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+            for (int r0 = 0; r0 < a.W; r0 += 8) {
+                float4 u0[8], u1[8];
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    if (r0 + uu < a.W) {
+                        const float *pp = sb + static_cast<int64_t>(r0 + uu) * Cfg::kSlotFloats +
+                                          (2 * jq) * 128;
+                        u0[uu] = ptx::ld_cg_f4(pp);
+                        u1[uu] = ptx::ld_cg_f4(pp + 128);
+                    }
+                }
+                // Fixed rank order: y = p_0, then y = y + p_r.
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu) {
+                    if (r0 + uu < a.W) {
+                        if (r0 + uu == 0) {
+                            y0 = u0[uu];
+                            y1 = u1[uu];
+                        } else {
+                            y0.x += u0[uu].x; y0.y += u0[uu].y; y0.z += u0[uu].z; y0.w += u0[uu].w;
+                            y1.x += u1[uu].x; y1.y += u1[uu].y; y1.z += u1[uu].z; y1.w += u1[uu].w;
+                        }
+                    }
+                }
+            }
+            const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + jq * 8;
+            if (row_ok && n < a.N) { // N is a multiple of 8
+                if (a.y_fp32) {
+                    float *yp = static_cast<float *>(a.Y) + m * a.N + n;
+                    ptx::st_f4(yp, y0);
+                    ptx::st_f4(yp + 4, y1);
+                } else {
+                    const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0.x, y0.y);
+                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(y0.z, y0.w);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(y1.x, y1.y);
+                    const __nv_bfloat162 h3 = __floats2bfloat162_rn(y1.z, y1.w);
+                    uint4 w;
+                    w.x = *reinterpret_cast<const uint32_t *>(&h0);
+                    w.y = *reinterpret_cast<const uint32_t *>(&h1);
+                    w.z = *reinterpret_cast<const uint32_t *>(&h2);
+                    w.w = *reinterpret_cast<const uint32_t *>(&h3);
+                    ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
+                }
+            }
+        }
+        // Every lane has read this slab of every rank.  The partials are dead
+        // until the next call rewrites them, so drop their L2 lines without
+        // write-back (lane l drops line l of each 4 KB block).
+        __syncwarp();
+        for (int r = 0; r < a.W; ++r)
+            ptx::discard_l2_line(qb + static_cast<int64_t>(r) * Cfg::kSlotFloats + slab * 1024 +
+                                 lane * 32);
+    }
+}
+
+// A consumer warp: claim entries until it takes a stop entry.
+template <int BN>
+__device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, int lane)
+{
+    const volatile int *abort_flag = &ctl->abort;
+    while (true) {
+        uint32_t n = 0;
+        int entry = -1, waited = 1;
+        if (lane == 0) {
+            n = atomicAdd(&ctl->rq_head, 1u);
+            const uint32_t s = n % kRQ;
+            const uint32_t ph = (n / kRQ) & 1u;
+            waited = ptx::mbar_wait(ptx::smem_u32(&ctl->rq_full[s]), ph, a.timeout, abort_flag) ? 1 : 0;
+            if (waited) {
+                entry = *reinterpret_cast<volatile int32_t *>(&ctl->rq_tile[s]);
+                ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_empty[s]));
+            }
+        }
+        waited = __shfl_sync(0xffffffffu, waited, 0);
+        entry = __shfl_sync(0xffffffffu, entry, 0);
+        if (!waited) {
+            if (lane == 0)
+                report(a, ctl, kStatusTimeoutReducer);
+            break;
+        }
+        if (entry < 0)
+            break;
+        reduce_quarter<BN>(a, entry >> 2, entry & 3, lane);
+    }
+}
+
 // ------------------------------------------------------------------ epilogue
 // PAIR: the CTA is half `crank` of a 256-row pair tile.  It drains its own
 // TMEM, waits with cluster-scope acquire, and hands the accumulator back to
@@ -394,121 +533,22 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 // Last arriver: the counter goes back to 0 for the next call
                 // (no memset), and the tile goes to the reducers.
                 ptx::st_relaxed_gpu(flag, 0u);
-                const uint32_t s = rq_n % kRQ;
-                const uint32_t ph = (rq_n / kRQ) & 1u;
-                if (ptx::mbar_wait(ptx::smem_u32(&ctl->rq_empty[s]), ph ^ 1u, a.timeout, abort_flag)) {
-                    ctl->rq_tile[s] = mt * a.nN + nt;
-                    ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_full[s]));
-                    ++rq_n;
-                } else {
-                    ok = false;
-                }
+                const int32_t tile = mt * a.nN + nt;
+                for (int qq = 0; qq < 4 && ok; ++qq)
+                    ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
             }
         }
     }
+    // No more tiles: one stop entry per consumer warp.
     if (etid == 0) {
-        if (ok) {
-            const uint32_t s = rq_n % kRQ;
-            const uint32_t ph = (rq_n / kRQ) & 1u;
-            if (ptx::mbar_wait(ptx::smem_u32(&ctl->rq_empty[s]), ph ^ 1u, a.timeout, abort_flag)) {
-                ctl->rq_tile[s] = -1; // no more tiles
-                ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_full[s]));
-            } else {
-                ok = false;
-            }
-        }
+        for (int i = 0; i < kConsumers && ok; ++i)
+            ok = rq_push(a, ctl, rq_n, -1);
         if (!ok)
             report(a, ctl, kStatusTimeoutEpilogue);
     }
-}
-
-// ------------------------------------------------------------------ reducer
-template <int BN>
-__device__ __forceinline__ void run_reducer(const KernelArgs &a, SmemCtl *ctl, int warp, int lane)
-{
-    using Cfg = TileCfg<BN>;
-    const volatile int *abort_flag = &ctl->abort;
-    const int q = warp - kRedWarp0; // rows [32q, 32q + 32) of the tile
-    uint32_t n_jobs = 0;
-    while (true) {
-        const uint32_t s = n_jobs % kRQ;
-        const uint32_t ph = (n_jobs / kRQ) & 1u;
-        int waited = 1;
-        if (lane == 0)
-            waited = ptx::mbar_wait(ptx::smem_u32(&ctl->rq_full[s]), ph, a.timeout, abort_flag) ? 1 : 0;
-        waited = __shfl_sync(0xffffffffu, waited, 0);
-        if (!waited) {
-            if (lane == 0)
-                report(a, ctl, kStatusTimeoutReducer);
-            break;
-        }
-        const int tile = *reinterpret_cast<volatile int32_t *>(&ctl->rq_tile[s]);
-        if (tile < 0)
-            break;
-        const int mt = tile / a.nN;
-        const int nt = tile - mt * a.nN;
-        const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
-        const bool row_ok = m < a.M;
-        const float *base = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
-                            static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
-#pragma unroll 1
-        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
-            const float *sb = base + slab * 1024;
-#pragma unroll 1
-            for (int jp = 0; jp < 4; ++jp) {
-                // Columns 8jp .. 8jp+7 of the slab: float4 j = 2jp and 2jp+1.
-                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-                for (int r0 = 0; r0 < a.W; r0 += 8) {
-                    float4 u0[8], u1[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (r0 + u < a.W) {
-                            const float *pp = sb + static_cast<int64_t>(r0 + u) * Cfg::kSlotFloats +
-                                              (2 * jp) * 128;
-                            u0[u] = ptx::ld_cg_f4(pp);
-                            u1[u] = ptx::ld_cg_f4(pp + 128);
-                        }
-                    }
-                    // Fixed rank order: y = p_0, then y = y + p_r.
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (r0 + u < a.W) {
-                            if (r0 + u == 0) {
-                                y0 = u0[u];
-                                y1 = u1[u];
-                            } else {
-                                y0.x += u0[u].x; y0.y += u0[u].y; y0.z += u0[u].z; y0.w += u0[u].w;
-                                y1.x += u1[u].x; y1.y += u1[u].y; y1.z += u1[u].z; y1.w += u1[u].w;
-                            }
-                        }
-                    }
-                }
-                const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + jp * 8;
-                if (row_ok && n < a.N) {
-                    if (a.y_fp32) {
-                        float *yp = static_cast<float *>(a.Y) + m * a.N + n;
-                        ptx::st_f4(yp, y0);
-                        ptx::st_f4(yp + 4, y1);
-                    } else {
-                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0.x, y0.y);
-                        const __nv_bfloat162 h1 = __floats2bfloat162_rn(y0.z, y0.w);
-                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(y1.x, y1.y);
-                        const __nv_bfloat162 h3 = __floats2bfloat162_rn(y1.z, y1.w);
-                        uint4 w;
-                        w.x = *reinterpret_cast<const uint32_t *>(&h0);
-                        w.y = *reinterpret_cast<const uint32_t *>(&h1);
-                        w.z = *reinterpret_cast<const uint32_t *>(&h2);
-                        w.w = *reinterpret_cast<const uint32_t *>(&h3);
-                        ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            ptx::mbar_arrive(ptx::smem_u32(&ctl->rq_empty[s]));
-        ++n_jobs;
-    }
+    // Once its own tiles are done, the epilogue helps with the reductions.
+    if (!ptx::named_bar_or(kBarEpi, 128, !ok))
+        run_consumer<BN>(a, ctl, lane);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -536,10 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kRQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 4);
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
+        ctl->rq_head = 0;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0 && a.nK > 0) {
@@ -567,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < kRedWarp0) {
         run_epilogue<BN, false>(a, sch, tmem, ctl, warp, lane, blockIdx.x, gridDim.x, 0u);
     } else {
-        run_reducer<BN>(a, ctl, warp, lane);
+        run_consumer<BN>(a, ctl, lane);
     }
 
     ptx::tc_fence_before();
@@ -759,10 +800,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kRQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 4);
+            ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
+        ctl->rq_head = 0;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0 && a.nK > 0) {
@@ -791,7 +833,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp < kRedWarp0) {
         run_epilogue<BN, true>(a, sch, tmem, ctl, warp, lane, blockIdx.x / 2, gridDim.x / 2, crank);
     } else {
-        run_reducer<BN>(a, ctl, warp, lane);
+        run_consumer<BN>(a, ctl, lane);
     }
 
     ptx::tc_fence_before();

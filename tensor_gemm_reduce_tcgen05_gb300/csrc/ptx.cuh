@@ -392,6 +392,20 @@ __device__ __forceinline__ void st_u4(void *p, uint4 v)
                  : "memory");
 }
 
+// Ask the TMA unit to bring [p, p + bytes) into L2 (bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Drop one 128-byte L2 line without writing it back.  Its contents become
+// undefined, so this is only for data that is dead: read for the last time,
+// and written again before it is next read.
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // 16-byte read-only load (C, the bias-like epilogue input).
 __device__ __forceinline__ uint4 ld_nc_u4(const void *p)
 {
