@@ -168,21 +168,26 @@ GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
 /*
  * The global tile order of the fused kernel, written to host memory `out` as
  * int32 triples (r, mt, nt) for entries g = 0 .. W*nM*nN-1, where
- * nM = ceil(M/bm) and nN = ceil(N/bn).  CTA b of a grid of G CTAs processes
- * entries b, b+G, b+2G, ...
+ * nM = ceil(M/bm) and nN = ceil(N/bn).  With bm = 256 (the CTA-pair kernel) a
+ * row tile is 256 rows.  Worker b of G workers (CTAs, or CTA pairs)
+ * processes entries b, b+G, b+2G, ...
  *   - Rank r visits its chunks in the order (r+1+s) mod W, s = 0 .. W-1:
  *     the remote chunks first and its own chunk r last
  *     ("flux实现：sm80 gemm+rs", section "gemmrs版本的swizzle如何编排").
  *     Each rank's start is offset by its rank ("flux精读" §4.1), so at every
  *     step the W ranks target W different chunks.
- *   - A row tile belongs to the chunk of its first row.  Inside a chunk, a
- *     rank walks the column tiles from offset (r*nN)/W.  For each column
- *     tile, it takes the chunk's row tiles in ascending order.
+ *   - A row tile belongs to the chunk of its first row.
+ *   - The column tiles, counted from offset (r*nN)/W, are split into groups of
+ *     `colgroup` tiles (0 or >= nN: one group).  For each group, the rank runs
+ *     all W steps.  Within a step it walks the group's column tiles forward on
+ *     even steps and backward on odd ones.  For each column tile it takes the
+ *     chunk's row tiles in ascending order.
  *   - Entry p*W + r is rank r's p-th tile: the ranks advance side by side.
  * `cap` is the capacity of `out` in triples.  Returns the number of entries,
  * or a negative error code (ERR_SHAPE if cap is too small).
  */
-GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *out, int64_t cap);
+GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup,
+                                     int32_t *out, int64_t cap);
 
 /*
  * Launch plan of the handle (host outputs; any pointer may be NULL):
@@ -190,7 +195,8 @@ GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn
  *   stages   depth of the TMA -> MMA shared-memory ring
  *   grid     CTAs launched (persistent: one per SM, at most one per work item)
  */
-GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid);
+GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
+                                 int *colgroup);
 
 /* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
  * (bm = 128).  Returns ERR_ARG for any other value. */
@@ -205,6 +211,12 @@ GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
  * kernel when there are at least four 256x256 rank-tiles per SM pair, otherwise
  * the widest single-CTA tile with at least four work items per SM. */
 GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
+
+/* Column tiles per schedule group (see gemm_rs_schedule).  0 (the default)
+ * means one group of all column tiles.  A smaller group shortens the time
+ * between a tile's first and last rank contribution, which keeps the partials
+ * in L2, at the cost of reading the A rows once per group. */
+GEMM_RS_API int gemm_rs_set_column_group(gemm_rs_t h, int colgroup);
 
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
 

@@ -181,15 +181,19 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
  *  - Output tiles are (mt, nt) with mt < ceil(M/BM) and nt < ceil(N/BN).
  *  - A tile belongs to the chunk of its first row: key(mt) = (mt*BM) / R.
  *  - Rank r visits chunks in the order (r+1+s) mod W for s = 0 .. W-1, so its
- *    own chunk r comes last.  Inside a chunk, it walks the column tiles
- *    starting at column offset (r*nN)/W, and for each column tile the chunk's
- *    row tiles in ascending order.
+ *    own chunk r comes last.
+ *  - The column tiles, counted from offset (r*nN)/W, form groups of G tiles
+ *    (G <= 0 or G >= nN: a single group).  For each group, in order, the rank
+ *    runs all W steps.  In step s it walks the group's column tiles forward
+ *    when s is even and backward when s is odd.  For each column tile it takes
+ *    the chunk's row tiles in ascending order.
  *  - The W ranks run side by side: entry p*W + r of the global order is the
  *    p-th tile of rank r.
  * Writes (r, mt, nt) triples to out[3*g .. 3*g+2].  Returns the number of
  * entries W*nM*nN, -1 on bad arguments, or -2 if cap (in entries) is too small.
  */
-int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int32_t *out, int64_t cap)
+int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int32_t *out,
+                        int64_t cap)
 {
     if (W < 1 || M < 1 || N < 1 || BM < 1 || BN < 1 || M % W != 0)
         return -1;
@@ -202,19 +206,24 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int32_t *ou
     int32_t *list = (int32_t *)malloc((size_t)T * 2 * sizeof(int32_t));
     if (list == NULL)
         return -1;
+    const int64_t group = (G <= 0 || G >= nN) ? nN : G;
     for (int r = 0; r < W; ++r) {
         int64_t p = 0;
         const int64_t rot = ((int64_t)r * nN) / W;
-        for (int s = 0; s < W; ++s) {
-            const int64_t c = (r + 1 + s) % W;
-            for (int64_t j = 0; j < nN; ++j) {
-                const int64_t nt = (j + rot) % nN;
-                for (int64_t mt = 0; mt < nM; ++mt) {
-                    if ((mt * BM) / R != c)
-                        continue;
-                    list[2 * p] = (int32_t)mt;
-                    list[2 * p + 1] = (int32_t)nt;
-                    ++p;
+        for (int64_t g0 = 0; g0 < nN; g0 += group) {
+            const int64_t gn = (nN - g0 < group) ? nN - g0 : group;
+            for (int s = 0; s < W; ++s) {
+                const int64_t c = (r + 1 + s) % W;
+                for (int64_t step_j = 0; step_j < gn; ++step_j) {
+                    const int64_t j = (s % 2 == 0) ? step_j : gn - 1 - step_j;
+                    const int64_t nt = (g0 + j + rot) % nN;
+                    for (int64_t mt = 0; mt < nM; ++mt) {
+                        if ((mt * BM) / R != c)
+                            continue;
+                        list[2 * p] = (int32_t)mt;
+                        list[2 * p + 1] = (int32_t)nt;
+                        ++p;
+                    }
                 }
             }
         }

@@ -239,6 +239,7 @@ struct gemm_rs_s {
     uint8_t *ws;
     Layout L;
     int device, sms, pair_clusters, bm, bn;
+    int colgroup; // 0: the default (one group)
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
     unsigned long long timeout;
@@ -308,6 +309,7 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->sms = sms;
     h->pair_clusters = pair_clusters;
     pick_tile(M, N, W, sms, &h->bm, &h->bn);
+    h->colgroup = 0;
     h->tmA_ptr = h->tmB_ptr = nullptr;
     h->timeout = 1ull << 32;
     h->record = nullptr;
@@ -322,7 +324,7 @@ int gemm_rs_destroy(gemm_rs_t h)
     return GEMM_RS_OK;
 }
 
-int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid)
+int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int *colgroup)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
@@ -333,6 +335,10 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid)
         *bn = h->bn;
     if (stages)
         *stages = stages_for(h->bm, h->bn);
+    if (colgroup) {
+        const int nN = static_cast<int>(cdiv(h->N, h->bn));
+        *colgroup = (h->colgroup <= 0 || h->colgroup > nN) ? nN : h->colgroup;
+    }
     if (grid) {
         if (h->bm == 2 * gemm_rs::kBM) {
             const int64_t pairs = h->pair_clusters;
@@ -365,6 +371,16 @@ int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn)
         return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not 128x{64,128,256} or 256x256", bm, bn);
     h->bm = bm;
     h->bn = bn;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_column_group(gemm_rs_t h, int colgroup)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (colgroup < 0)
+        return fail(GEMM_RS_ERR_ARG, "column group %d is negative", colgroup);
+    h->colgroup = colgroup;
     return GEMM_RS_OK;
 }
 
@@ -443,6 +459,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nN = static_cast<int>(cdiv(h->N, h->bn));
     a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
+    a.colgroup = (h->colgroup <= 0 || h->colgroup > a.nN) ? a.nN : h->colgroup;
     a.R = h->M / h->W;
     a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
@@ -522,7 +539,8 @@ int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream)
     return GEMM_RS_OK;
 }
 
-int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *out, int64_t cap)
+int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup, int32_t *out,
+                         int64_t cap)
 {
     if (W < 1 || W > 16)
         return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
@@ -532,8 +550,11 @@ int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int32_t *o
         return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not a tile of this library", bm, bn);
     if (out == nullptr)
         return fail(GEMM_RS_ERR_ARG, "out is NULL");
-    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), static_cast<int>(cdiv(N, bn)),
-                           bm == gemm_rs::kBM ? 7 : 8, M / W};
+    if (colgroup < 0)
+        return fail(GEMM_RS_ERR_ARG, "column group %d is negative", colgroup);
+    const int nN = static_cast<int>(cdiv(N, bn));
+    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), nN, bm == gemm_rs::kBM ? 7 : 8, M / W,
+                           (colgroup == 0 || colgroup > nN) ? nN : colgroup};
     const int64_t total = static_cast<int64_t>(W) * s.nM * s.nN;
     if (cap < total)
         return fail(GEMM_RS_ERR_SHAPE, "cap %lld < %lld entries", (long long)cap, (long long)total);
@@ -697,6 +718,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.nN = static_cast<int>(cdiv(N, bn));
     a.nK = static_cast<int>(cdiv(Kpr, gemm_rs::kBK));
     a.nMs = a.nM;
+    a.colgroup = a.nN;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

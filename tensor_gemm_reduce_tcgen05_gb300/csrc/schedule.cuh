@@ -9,10 +9,15 @@
 // first page: ReduceScatterOp<T, kM, kN, ...>): a row tile belongs to the
 // chunk of its first row, and the chunk shape need not match the tile shape.
 //
-// Inside a chunk, rank r walks the column tiles starting at (r*nN)/W.  For
-// each column tile it takes the chunk's row tiles in ascending order, so the
-// chunk's A rows stay in L2 while the column tiles go by.  The ranks advance
-// side by side: global entry g is rank (g mod W)'s (g / W)-th tile.
+// The order of one rank:
+//   for each column group (G column tiles; one group when G >= nN):
+//     for each step s = 0 .. W-1 (chunk (r+1+s) mod W):
+//       for each column tile of the group (forward on even steps and
+//       backward on odd ones, so that the B columns used last are used
+//       again first):
+//         for each row tile of the chunk, ascending.
+// Column tiles are counted from offset (r*nN)/W.  The ranks advance side by
+// side: global entry g is rank (g mod W)'s (g / W)-th tile.
 #pragma once
 
 #include <cstdint>
@@ -24,6 +29,7 @@ struct Sched {
     int nM, nN;
     int bm_shift; // log2(BM)
     int64_t R;    // rows per chunk, M / W
+    int G;        // column tiles per group (>= nN: one group)
 };
 
 __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
@@ -38,6 +44,12 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
     r = static_cast<int>(g % s.W);
     int64_t p = g / s.W;
     const int64_t rot = (static_cast<int64_t>(r) * s.nN) / s.W;
+    const int64_t G = s.G < s.nN ? s.G : s.nN;
+    // Every group but the last is full, so the group index follows directly.
+    const int64_t grp = p / (G * s.nM);
+    p -= grp * G * s.nM;
+    const int64_t g0 = grp * G;
+    const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
     for (int st = 0; st < s.W; ++st) {
         int c = r + 1 + st;
         if (c >= s.W)
@@ -48,12 +60,13 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
         const int64_t first = ceil_shift(static_cast<int64_t>(c) * s.R, s.bm_shift);
         const int64_t last = ceil_shift(static_cast<int64_t>(c + 1) * s.R, s.bm_shift);
         const int64_t cnt = last - first;
-        const int64_t items = cnt * s.nN;
+        const int64_t items = cnt * gn;
         if (p < items) {
-            const int64_t j = p / cnt;
-            const int64_t q = p - j * cnt;
+            const int64_t jl = p / cnt;
+            const int64_t q = p - jl * cnt;
             mt = static_cast<int>(first + q);
-            int64_t n = j + rot;
+            const int64_t j = (st & 1) ? gn - 1 - jl : jl;
+            int64_t n = g0 + j + rot;
             if (n >= s.nN)
                 n -= s.nN;
             nt = static_cast<int>(n);

@@ -52,13 +52,14 @@ def test_matches_printed_rank_offset_order():
         assert [seq[-1]] + seq[:-1] == order      # = printed order, local moved to the front
 
 
+@pytest.mark.parametrize("G", [0, 1, 3])
 @pytest.mark.parametrize("W,M,N,BM,BN", [
     (2, 256, 256, 128, 256), (8, 4096, 4096, 128, 256), (4, 16384, 5120, 128, 256),
     (8, 64, 8192, 128, 64), (3, 300, 520, 128, 128), (1, 200, 72, 128, 64),
-    (5, 5 * 128, 1000, 128, 256),
+    (5, 5 * 128, 1000, 128, 256), (8, 4096, 4096, 256, 256),
 ])
-def test_schedule_properties(W, M, N, BM, BN):
-    sched = oracle.schedule(W, M, N, BM, BN)
+def test_schedule_properties(W, M, N, BM, BN, G):
+    sched = oracle.schedule(W, M, N, BM, BN, G)
     nM, nN = -(-M // BM), -(-N // BN)
     assert sched.shape == (W * nM * nN, 3)
     # every rank-tile exactly once
@@ -68,11 +69,15 @@ def test_schedule_properties(W, M, N, BM, BN):
     # ranks run side by side
     assert np.array_equal(sched[:, 0], np.tile(np.arange(W), nM * nN))
     R = M // W
+    groups = 1 if G <= 0 or G >= nN else -(-nN // G)
     for r in range(W):
         seq = _chunk_sequence(sched, W, M, BM, r)
-        expect = [(r + 1 + s) % W for s in range(W)]
         present = {(mt * BM) // R for mt in range(nM)}
-        assert seq == [c for c in expect if c in present]
+        expect = [c for c in [(r + 1 + s) % W for s in range(W)] if c in present]
+        if len(expect) == 1:
+            assert seq == expect
+        else:
+            assert seq == expect * groups  # remote chunks first, local last, in every group
     if R % BM == 0:
         # every position p: the W ranks target W distinct chunks
         per_p = sched.reshape(nM * nN, W, 3)
@@ -81,11 +86,34 @@ def test_schedule_properties(W, M, N, BM, BN):
             assert len(chunks) == W
 
 
+def test_serpentine_column_order_between_steps():
+    """Consecutive steps walk the column tiles in opposite directions, so a
+    rank's last column tile of one step is its first of the next."""
+    W, M, N, BM, BN = 4, 4 * 128, 2048, 128, 256
+    sched = oracle.schedule(W, M, N, BM, BN)
+    nN = N // BN
+    for r in range(W):
+        cols = [int(nt) for (rr, mt, nt) in sched if rr == r]
+        steps = [cols[s * nN:(s + 1) * nN] for s in range(W)]
+        rot = (r * nN) // W
+        assert steps[0] == [(j + rot) % nN for j in range(nN)]
+        for s in range(1, W):
+            assert steps[s] == steps[s - 1][::-1]
+
+
 def test_rank_column_offset_when_one_chunk_holds_all_tiles():
-    """M = 64, W = 8: chunks of 8 rows, one row tile.  The ranks then start
-    on different column tiles."""
+    """M = 64, W = 8: chunks of 8 rows, one row tile (keyed to chunk 0).  Rank
+    r reaches chunk 0 at step s = W-1-r.  It starts at column (r*nN)/W, or
+    walks backwards from the column before it when s is odd, so the ranks
+    start on different column tiles."""
     W, M, N, BM, BN = 8, 64, 8192, 128, 64
     sched = oracle.schedule(W, M, N, BM, BN)
     nN = N // BN
     first = sched[:W]
-    assert first[:, 2].tolist() == [(r * nN) // W for r in range(W)]
+    expect = []
+    for r in range(W):
+        rot = (r * nN) // W
+        s = (0 - r - 1) % W
+        expect.append(rot if s % 2 == 0 else (rot + nN - 1) % nN)
+    assert first[:, 2].tolist() == expect
+    assert len(set(expect)) == W
