@@ -179,24 +179,27 @@ GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
  *   - A row tile belongs to the chunk of its first row.
  *   - The column tiles, counted from offset (r*nN)/W, are split into groups of
  *     `colgroup` tiles (0 or >= nN: one group).  For each group, the rank runs
- *     all W steps.  Within a step it walks the group's column tiles forward on
- *     even steps and backward on odd ones.  For each column tile it takes the
- *     chunk's row tiles in ascending order.
+ *     all W steps.  In a step, the chunk's row tiles (ascending) are split into
+ *     row groups of `rowgroup` tiles (0: the whole chunk).  Each row group is one
+ *     sweep over the column group's tiles.  Sweeps, counted from the start of
+ *     the column group, go forward when even and backward when odd.  For each
+ *     column tile a sweep takes the row group's tiles in ascending order.
  *   - Entry p*W + r is rank r's p-th tile: the ranks advance side by side.
  * `cap` is the capacity of `out` in triples.  Returns the number of entries,
  * or a negative error code (ERR_SHAPE if cap is too small).
  */
 GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup,
-                                     int32_t *out, int64_t cap);
+                                     int rowgroup, int32_t *out, int64_t cap);
 
 /*
  * Launch plan of the handle (host outputs; any pointer may be NULL):
  *   bm, bn   the output tile (bm = 128; bn = 256, 128 or 64)
  *   stages   depth of the TMA -> MMA shared-memory ring
  *   grid     CTAs launched (persistent: one per SM, at most one per work item)
+ *   colgroup, rowgroup  the schedule shape in effect (see gemm_rs_set_schedule)
  */
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
-                                 int *colgroup);
+                                 int *colgroup, int *rowgroup);
 
 /* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
  * (bm = 128).  Returns ERR_ARG for any other value. */
@@ -212,11 +215,16 @@ GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
  * the widest single-CTA tile with at least four work items per SM. */
 GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
 
-/* Column tiles per schedule group (see gemm_rs_schedule).  0 (the default)
- * means one group of all column tiles.  A smaller group shortens the time
- * between a tile's first and last rank contribution, which keeps the partials
- * in L2, at the cost of reading the A rows once per group. */
-GEMM_RS_API int gemm_rs_set_column_group(gemm_rs_t h, int colgroup);
+/* Schedule shape (see gemm_rs_schedule).
+ *   colgroup  column tiles per column group.  0 (the default) = one group of
+ *             all column tiles.  A smaller group shortens the time between a
+ *             tile's first and last rank contribution, at the cost of reading
+ *             the A rows once per group.
+ *   rowgroup  row tiles per column sweep.  0 (the default) = the library's
+ *             choice: as many as keep about 48 MB of A rows (all ranks) live,
+ *             capped at the chunk.  Smaller groups re-read B once per sweep.
+ * Returns ERR_ARG for negative values. */
+GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup);
 
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
 

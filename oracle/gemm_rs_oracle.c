@@ -184,16 +184,18 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
  *    own chunk r comes last.
  *  - The column tiles, counted from offset (r*nN)/W, form groups of G tiles
  *    (G <= 0 or G >= nN: a single group).  For each group, in order, the rank
- *    runs all W steps.  In step s it walks the group's column tiles forward
- *    when s is even and backward when s is odd.  For each column tile it takes
- *    the chunk's row tiles in ascending order.
+ *    runs all W steps.  In a step, the chunk's row tiles (ascending) are split
+ *    into row groups of RG tiles (RG <= 0: the whole chunk).  Each row group is
+ *    one sweep over the group's column tiles.  Sweeps, counted from the start of
+ *    the column group, go forward when even and backward when odd.  For each
+ *    column tile a sweep takes the row group's tiles in ascending order.
  *  - The W ranks run side by side: entry p*W + r of the global order is the
  *    p-th tile of rank r.
  * Writes (r, mt, nt) triples to out[3*g .. 3*g+2].  Returns the number of
  * entries W*nM*nN, -1 on bad arguments, or -2 if cap (in entries) is too small.
  */
-int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int32_t *out,
-                        int64_t cap)
+int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int RG,
+                        int32_t *out, int64_t cap)
 {
     if (W < 1 || M < 1 || N < 1 || BM < 1 || BN < 1 || M % W != 0)
         return -1;
@@ -204,31 +206,45 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int3
     if (cap < W * T)
         return -2;
     int32_t *list = (int32_t *)malloc((size_t)T * 2 * sizeof(int32_t));
-    if (list == NULL)
+    int64_t *rows = (int64_t *)malloc((size_t)nM * sizeof(int64_t));
+    if (list == NULL || rows == NULL) {
+        free(list);
+        free(rows);
         return -1;
+    }
     const int64_t group = (G <= 0 || G >= nN) ? nN : G;
     for (int r = 0; r < W; ++r) {
         int64_t p = 0;
         const int64_t rot = ((int64_t)r * nN) / W;
         for (int64_t g0 = 0; g0 < nN; g0 += group) {
             const int64_t gn = (nN - g0 < group) ? nN - g0 : group;
+            int64_t sweep = 0;
             for (int s = 0; s < W; ++s) {
                 const int64_t c = (r + 1 + s) % W;
-                for (int64_t step_j = 0; step_j < gn; ++step_j) {
-                    const int64_t j = (s % 2 == 0) ? step_j : gn - 1 - step_j;
-                    const int64_t nt = (g0 + j + rot) % nN;
-                    for (int64_t mt = 0; mt < nM; ++mt) {
-                        if ((mt * BM) / R != c)
-                            continue;
-                        list[2 * p] = (int32_t)mt;
-                        list[2 * p + 1] = (int32_t)nt;
-                        ++p;
+                /* the chunk's row tiles, ascending */
+                int64_t n_rows = 0;
+                for (int64_t mt = 0; mt < nM; ++mt)
+                    if ((mt * BM) / R == c)
+                        rows[n_rows++] = mt;
+                const int64_t rgs = (RG <= 0 || RG > n_rows) ? n_rows : RG;
+                for (int64_t r0 = 0; r0 < n_rows; r0 += rgs) {
+                    const int64_t r1 = (r0 + rgs < n_rows) ? r0 + rgs : n_rows;
+                    for (int64_t step_j = 0; step_j < gn; ++step_j) {
+                        const int64_t j = (sweep % 2 == 0) ? step_j : gn - 1 - step_j;
+                        const int64_t nt = (g0 + j + rot) % nN;
+                        for (int64_t i = r0; i < r1; ++i) {
+                            list[2 * p] = (int32_t)rows[i];
+                            list[2 * p + 1] = (int32_t)nt;
+                            ++p;
+                        }
                     }
+                    ++sweep;
                 }
             }
         }
         if (p != T) {
             free(list);
+            free(rows);
             return -1;
         }
         for (int64_t q = 0; q < T; ++q) {
@@ -239,5 +255,6 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int3
         }
     }
     free(list);
+    free(rows);
     return W * T;
 }

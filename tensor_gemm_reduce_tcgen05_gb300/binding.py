@@ -70,11 +70,9 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_last_error": (ctypes.c_char_p, []),
             "gemm_rs_status": (i32, [vp, vp]),
             "gemm_rs_reset": (i32, [vp, vp]),
-            "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, i32, vp, i64]),
-            "gemm_rs_get_plan": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                       ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                       ctypes.POINTER(i32)]),
-            "gemm_rs_set_column_group": (i32, [vp, i32]),
+            "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, i32, i32, vp, i64]),
+            "gemm_rs_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 6),
+            "gemm_rs_set_schedule": (i32, [vp, i32, i32]),
             "gemm_rs_set_tile_n": (i32, [vp, i32]),
             "gemm_rs_set_tile": (i32, [vp, i32, i32]),
             "gemm_rs_set_timeout_cycles": (i32, [vp, u64]),
@@ -138,21 +136,24 @@ def gemm_rs_reset(h, stream=0) -> None:
     _check(lib().gemm_rs_reset(h, stream))
 
 
-def gemm_rs_schedule(M: int, N: int, W: int, bm: int, bn: int, colgroup: int = 0) -> np.ndarray:
+def gemm_rs_schedule(M: int, N: int, W: int, bm: int, bn: int, colgroup: int = 0,
+                     rowgroup: int = 0) -> np.ndarray:
     nM, nN = -(-M // bm), -(-N // bn)
     out = np.zeros((W * nM * nN, 3), dtype=np.int32)
-    n = _check(lib().gemm_rs_schedule(M, N, W, bm, bn, colgroup, out.ctypes.data, out.shape[0]))
+    n = _check(lib().gemm_rs_schedule(M, N, W, bm, bn, colgroup, rowgroup, out.ctypes.data,
+                                      out.shape[0]))
     return out[:n]
 
 
 def gemm_rs_get_plan(h) -> dict:
-    v = [ctypes.c_int() for _ in range(5)]
+    v = [ctypes.c_int() for _ in range(6)]
     _check(lib().gemm_rs_get_plan(h, *[ctypes.byref(x) for x in v]))
-    return dict(zip(("bm", "bn", "stages", "grid", "colgroup"), (x.value for x in v)))
+    return dict(zip(("bm", "bn", "stages", "grid", "colgroup", "rowgroup"),
+                    (x.value for x in v)))
 
 
-def gemm_rs_set_column_group(h, colgroup: int) -> None:
-    _check(lib().gemm_rs_set_column_group(h, colgroup))
+def gemm_rs_set_schedule(h, colgroup: int = 0, rowgroup: int = 0) -> None:
+    _check(lib().gemm_rs_set_schedule(h, colgroup, rowgroup))
 
 
 def gemm_rs_set_tile_n(h, bn: int) -> None:

@@ -229,6 +229,22 @@ void pick_tile(int64_t M, int64_t N, int W, int sms, int *bm, int *bn)
     *bn = pick_bn(M, N, W, sms);
 }
 
+// Row tiles per column sweep.  A sweep keeps its row tiles' A rows live in
+// L2 for every rank at once, so bound them to about 48 MB across the W ranks.
+// Returns the chunk's row tile count (one sweep per step) when that fits.
+int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm)
+{
+    const int64_t rows_per_chunk = cdiv(M / W, bm) + 1;
+    const int64_t panel = static_cast<int64_t>(bm) * Kpr * 2 * W;
+    if (panel <= 0)
+        return static_cast<int>(rows_per_chunk);
+    const int64_t budget = int64_t(48) << 20;
+    int64_t rg = budget / panel;
+    if (rg < 1)
+        rg = 1;
+    return static_cast<int>(rg < rows_per_chunk ? rg : rows_per_chunk);
+}
+
 } // namespace
 
 struct gemm_rs_s {
@@ -239,7 +255,8 @@ struct gemm_rs_s {
     uint8_t *ws;
     Layout L;
     int device, sms, pair_clusters, bm, bn;
-    int colgroup; // 0: the default (one group)
+    int colgroup; // 0: one group of all column tiles
+    int rowgroup; // 0: the default (pick_rowgroup)
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
     unsigned long long timeout;
@@ -310,6 +327,7 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->pair_clusters = pair_clusters;
     pick_tile(M, N, W, sms, &h->bm, &h->bn);
     h->colgroup = 0;
+    h->rowgroup = 0;
     h->tmA_ptr = h->tmB_ptr = nullptr;
     h->timeout = 1ull << 32;
     h->record = nullptr;
@@ -324,7 +342,8 @@ int gemm_rs_destroy(gemm_rs_t h)
     return GEMM_RS_OK;
 }
 
-int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int *colgroup)
+int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int *colgroup,
+                     int *rowgroup)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
@@ -339,6 +358,8 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int 
         const int nN = static_cast<int>(cdiv(h->N, h->bn));
         *colgroup = (h->colgroup <= 0 || h->colgroup > nN) ? nN : h->colgroup;
     }
+    if (rowgroup)
+        *rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
     if (grid) {
         if (h->bm == 2 * gemm_rs::kBM) {
             const int64_t pairs = h->pair_clusters;
@@ -374,13 +395,15 @@ int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn)
     return GEMM_RS_OK;
 }
 
-int gemm_rs_set_column_group(gemm_rs_t h, int colgroup)
+int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
-    if (colgroup < 0)
-        return fail(GEMM_RS_ERR_ARG, "column group %d is negative", colgroup);
+    if (colgroup < 0 || rowgroup < 0)
+        return fail(GEMM_RS_ERR_ARG, "column group %d / row group %d is negative", colgroup,
+                    rowgroup);
     h->colgroup = colgroup;
+    h->rowgroup = rowgroup;
     return GEMM_RS_OK;
 }
 
@@ -460,6 +483,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
     a.colgroup = (h->colgroup <= 0 || h->colgroup > a.nN) ? a.nN : h->colgroup;
+    a.rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
     a.R = h->M / h->W;
     a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
@@ -539,8 +563,8 @@ int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream)
     return GEMM_RS_OK;
 }
 
-int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup, int32_t *out,
-                         int64_t cap)
+int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup, int rowgroup,
+                         int32_t *out, int64_t cap)
 {
     if (W < 1 || W > 16)
         return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
@@ -550,11 +574,14 @@ int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgro
         return fail(GEMM_RS_ERR_ARG, "tile %dx%d is not a tile of this library", bm, bn);
     if (out == nullptr)
         return fail(GEMM_RS_ERR_ARG, "out is NULL");
-    if (colgroup < 0)
-        return fail(GEMM_RS_ERR_ARG, "column group %d is negative", colgroup);
+    if (colgroup < 0 || rowgroup < 0)
+        return fail(GEMM_RS_ERR_ARG, "column group %d / row group %d is negative", colgroup,
+                    rowgroup);
     const int nN = static_cast<int>(cdiv(N, bn));
-    const gemm_rs::Sched s{W, static_cast<int>(cdiv(M, bm)), nN, bm == gemm_rs::kBM ? 7 : 8, M / W,
-                           (colgroup == 0 || colgroup > nN) ? nN : colgroup};
+    const int nMs = static_cast<int>(cdiv(M, bm));
+    const gemm_rs::Sched s{W, nMs, nN, bm == gemm_rs::kBM ? 7 : 8, M / W,
+                           (colgroup == 0 || colgroup > nN) ? nN : colgroup,
+                           rowgroup == 0 ? nMs : rowgroup};
     const int64_t total = static_cast<int64_t>(W) * s.nM * s.nN;
     if (cap < total)
         return fail(GEMM_RS_ERR_SHAPE, "cap %lld < %lld entries", (long long)cap, (long long)total);
@@ -719,6 +746,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.nK = static_cast<int>(cdiv(Kpr, gemm_rs::kBK));
     a.nMs = a.nM;
     a.colgroup = a.nN;
+    a.rowgroup = a.nM;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

@@ -105,6 +105,7 @@ struct KernelArgs {
     int W, M, N, nM, nN, nK;
     int nMs;        // row tiles of the schedule (nM, or ceil(M/256) for CTA pairs)
     int colgroup;   // column tiles per schedule group (>= nN: one group)
+    int rowgroup;   // row tiles per sweep (>= a chunk's row tiles: one sweep per step)
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const Sched sch{a.W, a.nMs, a.nN, 7, a.R, a.colgroup};
+    const Sched sch{a.W, a.nMs, a.nN, 7, a.R, a.colgroup, a.rowgroup};
 
     if (warp == 0) {
         if (lane == 0)
@@ -821,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cluster_sync(); // the peer's barriers are initialised before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const Sched sch{a.W, a.nMs, a.nN, 8, a.R, a.colgroup};
+    const Sched sch{a.W, a.nMs, a.nN, 8, a.R, a.colgroup, a.rowgroup};
 
     if (warp == 0) {
         if (lane == 0)

@@ -12,12 +12,17 @@
 // The order of one rank:
 //   for each column group (G column tiles; one group when G >= nN):
 //     for each step s = 0 .. W-1 (chunk (r+1+s) mod W):
-//       for each column tile of the group (forward on even steps and
-//       backward on odd ones, so that the B columns used last are used
-//       again first):
-//         for each row tile of the chunk, ascending.
-// Column tiles are counted from offset (r*nN)/W.  The ranks advance side by
-// side: global entry g is rank (g mod W)'s (g / W)-th tile.
+//       for each row group of the chunk (RG row tiles; one group when RG
+//       covers the chunk):
+//         one sweep over the column tiles of the column group, forward on
+//         even sweeps and backward on odd ones (sweeps counted from the start
+//         of the column group), so that the B columns used last are the
+//         first used again;
+//           for each row tile of the row group, ascending.
+// Column tiles are counted from offset (r*nN)/W.  Row groups bound the A rows
+// a sweep keeps live, so they can stay in L2 while the columns go by.  The
+// ranks advance side by side: global entry g is rank (g mod W)'s (g / W)-th
+// tile.
 #pragma once
 
 #include <cstdint>
@@ -30,6 +35,7 @@ struct Sched {
     int bm_shift; // log2(BM)
     int64_t R;    // rows per chunk, M / W
     int G;        // column tiles per group (>= nN: one group)
+    int RG;       // row tiles per row group (>= a chunk's row tiles: one group)
 };
 
 __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
@@ -50,6 +56,7 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
     p -= grp * G * s.nM;
     const int64_t g0 = grp * G;
     const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
+    int64_t sweep = 0; // column sweeps before the current step
     for (int st = 0; st < s.W; ++st) {
         int c = r + 1 + st;
         if (c >= s.W)
@@ -61,11 +68,15 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
         const int64_t last = ceil_shift(static_cast<int64_t>(c + 1) * s.R, s.bm_shift);
         const int64_t cnt = last - first;
         const int64_t items = cnt * gn;
+        const int64_t RG = s.RG < cnt ? s.RG : cnt;
         if (p < items) {
-            const int64_t jl = p / cnt;
-            const int64_t q = p - jl * cnt;
-            mt = static_cast<int>(first + q);
-            const int64_t j = (st & 1) ? gn - 1 - jl : jl;
+            // Every row group but the chunk's last is full.
+            const int64_t rg = p / (RG * gn);
+            const int64_t q = p - rg * RG * gn;
+            const int64_t rn = (cnt - rg * RG) < RG ? (cnt - rg * RG) : RG;
+            const int64_t jl = q / rn;
+            mt = static_cast<int>(first + rg * RG + (q - jl * rn));
+            const int64_t j = ((sweep + rg) & 1) ? gn - 1 - jl : jl;
             int64_t n = g0 + j + rot;
             if (n >= s.nN)
                 n -= s.nN;
@@ -73,6 +84,8 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
             return;
         }
         p -= items;
+        if (cnt > 0)
+            sweep += (cnt + RG - 1) / RG;
     }
     mt = -1;
     nt = -1;

@@ -51,13 +51,13 @@ def test_version(b):
     (16, 16 * 7, 64, 64), (7, 7 * 129, 264, 128),
 ])
 def test_schedule_matches_oracle(b, W, M, N, bn):
-    for G in (0, 1, 2, 5):
-        ours = b.gemm_rs_schedule(M, N, W, 128, bn, G)
-        ref = oracle.schedule(W, M, N, 128, bn, G)
+    for G, RG in ((0, 0), (1, 0), (2, 3), (5, 1), (0, 2), (3, 5)):
+        ours = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG)
+        ref = oracle.schedule(W, M, N, 128, bn, G, RG)
         np.testing.assert_array_equal(ours, ref)
         # the CTA-pair kernel walks 256-row tiles
-        np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256, G),
-                                      oracle.schedule(W, M, N, 256, 256, G))
+        np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256, G, RG),
+                                      oracle.schedule(W, M, N, 256, 256, G, RG))
 
 
 def test_workspace_bytes(b):

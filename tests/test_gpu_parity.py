@@ -129,24 +129,28 @@ def test_twenty_calls_bit_identical_and_counters_reset():
 
 def test_device_schedule_record_matches_schedule_and_oracle():
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
-    for (W, M, N, Kpr, bm, bn, G) in [(8, 1024, 1024, 64, 128, 256, 0),
-                                      (3, 300, 520, 64, 128, 128, 2),
-                                      (8, 64, 8192, 64, 128, 64, 0),
-                                      (8, 4096, 1024, 64, 256, 256, 0),
-                                      (8, 4096, 2048, 64, 256, 256, 3),
-                                      (3, 300, 520, 64, 256, 256, 1)]:
+    for (W, M, N, Kpr, bm, bn, G, RG) in [(8, 1024, 1024, 64, 128, 256, 0, 0),
+                                          (3, 300, 520, 64, 128, 128, 2, 1),
+                                          (8, 64, 8192, 64, 128, 64, 0, 0),
+                                          (8, 4096, 1024, 64, 256, 256, 0, 0),
+                                          (8, 4096, 2048, 64, 256, 256, 3, 1),
+                                          (4, 4096, 2048, 64, 256, 256, 0, 3),
+                                          (3, 300, 520, 64, 256, 256, 1, 0)]:
         A, B, _ = inputs(W, M, N, Kpr, "int")
         op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_m=bm, tile_n=bn)
-        b.gemm_rs_set_column_group(op.handle, G)
+        b.gemm_rs_set_schedule(op.handle, G, RG)
         nM, nN = -(-M // bm), -(-N // bn)
         rec = torch.full((W * nM * nN, 4), -1, dtype=torch.int32, device="cuda:0")
         b.gemm_rs_set_debug(op.handle, rec.data_ptr(), 0)
         Y = op.run(A.cuda(), B.cuda())
         torch.cuda.synchronize()
         rec = rec.cpu().numpy()
-        lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn, G)
+        plan = op.plan
+        lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn, plan["colgroup"], plan["rowgroup"])
         np.testing.assert_array_equal(rec[:, :3], lib_sched)
-        np.testing.assert_array_equal(rec[:, :3], oracle.schedule(W, M, N, bm, bn, G))
+        np.testing.assert_array_equal(rec[:, :3],
+                                      oracle.schedule(W, M, N, bm, bn, plan["colgroup"],
+                                                      plan["rowgroup"]))
         grid = op.plan["grid"]
         workers = grid // 2 if bm == 256 else grid  # CTA pairs process one entry each
         np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % workers)

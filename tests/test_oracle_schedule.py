@@ -52,14 +52,14 @@ def test_matches_printed_rank_offset_order():
         assert [seq[-1]] + seq[:-1] == order      # = printed order, local moved to the front
 
 
-@pytest.mark.parametrize("G", [0, 1, 3])
+@pytest.mark.parametrize("G,RG", [(0, 0), (1, 0), (3, 0), (0, 1), (2, 3)])
 @pytest.mark.parametrize("W,M,N,BM,BN", [
     (2, 256, 256, 128, 256), (8, 4096, 4096, 128, 256), (4, 16384, 5120, 128, 256),
     (8, 64, 8192, 128, 64), (3, 300, 520, 128, 128), (1, 200, 72, 128, 64),
     (5, 5 * 128, 1000, 128, 256), (8, 4096, 4096, 256, 256),
 ])
-def test_schedule_properties(W, M, N, BM, BN, G):
-    sched = oracle.schedule(W, M, N, BM, BN, G)
+def test_schedule_properties(W, M, N, BM, BN, G, RG):
+    sched = oracle.schedule(W, M, N, BM, BN, G, RG)
     nM, nN = -(-M // BM), -(-N // BN)
     assert sched.shape == (W * nM * nN, 3)
     # every rank-tile exactly once
@@ -101,6 +101,25 @@ def test_serpentine_column_order_between_steps():
             assert steps[s] == steps[s - 1][::-1]
 
 
+def test_row_groups_sweep_all_columns_per_group():
+    """With row groups of 2 row tiles, a step of a 6-tile chunk makes three
+    sweeps over the column tiles, alternating direction, each covering its
+    two row tiles for every column."""
+    W, M, N, BM, BN, RG = 2, 2 * 6 * 128, 1024, 128, 256, 2
+    sched = oracle.schedule(W, M, N, BM, BN, 0, RG)
+    nN = N // BN
+    mine = [(int(mt), int(nt)) for (rr, mt, nt) in sched if rr == 0]
+    step0 = mine[:6 * nN]              # rank 0, step 0: chunk 1 (row tiles 6..11)
+    rot = 0
+    for k in range(3):
+        sweep = step0[k * 2 * nN:(k + 1) * 2 * nN]
+        cols = [sweep[2 * i][1] for i in range(nN)]
+        fwd = [(j + rot) % nN for j in range(nN)]
+        assert cols == (fwd if k % 2 == 0 else fwd[::-1])
+        for i in range(nN):
+            assert [sweep[2 * i][0], sweep[2 * i + 1][0]] == [6 + 2 * k, 7 + 2 * k]
+
+
 def test_rank_column_offset_when_one_chunk_holds_all_tiles():
     """M = 64, W = 8: chunks of 8 rows, one row tile (keyed to chunk 0).  Rank
     r reaches chunk 0 at step s = W-1-r.  It starts at column (r*nN)/W, or
@@ -112,8 +131,6 @@ def test_rank_column_offset_when_one_chunk_holds_all_tiles():
     first = sched[:W]
     expect = []
     for r in range(W):
-        rot = (r * nN) // W
-        s = (0 - r - 1) % W
-        expect.append(rot if s % 2 == 0 else (rot + nN - 1) % nN)
+        expect.append((r * nN) // W)  # one sweep per rank, forward
     assert first[:, 2].tolist() == expect
     assert len(set(expect)) == W
