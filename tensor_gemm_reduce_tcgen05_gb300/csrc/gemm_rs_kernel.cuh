@@ -323,19 +323,8 @@ __device__ __forceinline__ void reduce_quarter(const KernelArgs &a, int tile, in
     // rank 0's 32-row quarter; rank r's is kSlotFloats further on
     const float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                       static_cast<int64_t>(q) * S * 1024;
-    // Lane r < W prefetches rank r's 4 KB block of a slab into L2, two slabs
-    // ahead of the loads.
-    const bool pf_lane = lane < a.W;
-    const float *pf_base = qb + static_cast<int64_t>(pf_lane ? lane : 0) * Cfg::kSlotFloats;
-    if (pf_lane) {
-        ptx::bulk_prefetch_l2(pf_base, 4096);
-        if (S > 1)
-            ptx::bulk_prefetch_l2(pf_base + 1024, 4096);
-    }
 #pragma unroll 1
     for (int slab = 0; slab < S; ++slab) {
-        if (pf_lane && slab + 2 < S)
-            ptx::bulk_prefetch_l2(pf_base + (slab + 2) * 1024, 4096);
         const float *sb = qb + slab * 1024 + lane * 4;
 #pragma unroll 1
         for (int jq = 0; jq < 4; ++jq) {
@@ -441,6 +430,9 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     const int q = warp & 3;                           // TMEM lanes [32q, 32q + 32)
     const int etid = threadIdx.x - kEpiWarp0 * 32;    // 0 .. 127
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    // Partials are read back only at the end of the schedule: do not let them
+    // push the B panels out of L2.
+    const uint64_t st_pol = ptx::policy_evict_first();
     bool ok = true;
     uint32_t rq_n = 0;
     int it = 0;
@@ -521,7 +513,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             float *dst = slot + slab * 1024;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                ptx::st_f4(dst + j * 128, make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+                ptx::st_f4_hint(dst + j * 128,
+                                make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]), st_pol);
         }
 
         // Every epilogue thread has issued its stores.  Publish them at gpu
@@ -632,7 +625,8 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
 {
     using Cfg = PairCfg<BN>;
     const volatile int *abort_flag = &ctl->abort;
-    const uint64_t pol = ptx::policy_evict_normal();
+    const uint64_t polA = ptx::policy_evict_normal();
+    const uint64_t polB = ptx::policy_evict_last(); // B panels are swept again every step
     const int64_t ncl = gridDim.x / 2;
     const int64_t cid = blockIdx.x / 2;
     uint32_t stage = 0, phase = 0;
@@ -661,11 +655,11 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
                 const uint32_t fb_leader = ptx::mapa(fb, 0);
                 const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
                 ptx::tma_load_3d_pair(sa, tmA, fb_leader, kb * kBK, mt2 * (2 * kBM) + crank * kBM, r,
-                                      pol);
+                                      polA);
 #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)
                     ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
-                                          nt * BN + crank * (BN / 2) + j * 64, kb * kBK, r, pol);
+                                          nt * BN + crank * (BN / 2) + j * 64, kb * kBK, r, polB);
                 ++issued;
                 if (++stage == Cfg::kStages) {
                     stage = 0;

@@ -392,10 +392,19 @@ __device__ __forceinline__ void st_u4(void *p, uint4 v)
                  : "memory");
 }
 
-// Ask the TMA unit to bring [p, p + bytes) into L2 (bytes a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+__device__ __forceinline__ uint64_t policy_evict_first()
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16-byte store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_f4_hint(float *p, float4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
 }
 
 // Drop one 128-byte L2 line without writing it back.  Its contents become
