@@ -83,6 +83,19 @@ enum {
     GEMM_RS_ERR_WORKSPACE = -7    /* workspace smaller than gemm_rs_workspace_bytes() */
 };
 
+/* How the W partials of an output tile are reduced (gemm_rs_set_reduce_mode). */
+enum {
+    /* Default.  The ranks fold into the tile in the order of the steps at which
+     * they reach it (a fixed order per tile).  The rank whose turn it is adds
+     * its accumulator straight from TMEM onto the running sum.  A rank that is
+     * early stores its partial, and the current owner of the fold picks it up.
+     * The rank at the last step writes Y.  The reduction overlaps the GEMM. */
+    GEMM_RS_REDUCE_CHAIN = 0,
+    /* Every rank stores its partial.  The last rank to arrive at a tile folds
+     * all W partials in rank order 0 .. W-1 and writes Y. */
+    GEMM_RS_REDUCE_LAST_ARRIVER = 1
+};
+
 /* Debug flags for gemm_rs_set_debug. */
 enum {
     /* The TMA producer issues no loads, so the MMA warp's wait on the first
@@ -177,13 +190,12 @@ GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
  *     Each rank's start is offset by its rank ("flux精读" §4.1), so at every
  *     step the W ranks target W different chunks.
  *   - A row tile belongs to the chunk of its first row.
- *   - The column tiles, counted from offset (r*nN)/W, are split into groups of
+ *   - The column tiles, counted from offset ((W-r) mod W)*nN/W, are split into groups of
  *     `colgroup` tiles (0 or >= nN: one group).  For each group, the rank runs
  *     all W steps.  In a step, the chunk's row tiles (ascending) are split into
  *     row groups of `rowgroup` tiles (0: the whole chunk).  Each row group is one
- *     sweep over the column group's tiles.  Sweeps, counted from the start of
- *     the column group, go forward when even and backward when odd.  For each
- *     column tile a sweep takes the row group's tiles in ascending order.
+ *     forward sweep over the column group's tiles.  For each column tile a
+ *     sweep takes the row group's tiles in ascending order.
  *   - Entry p*W + r is rank r's p-th tile: the ranks advance side by side.
  * `cap` is the capacity of `out` in triples.  Returns the number of entries,
  * or a negative error code (ERR_SHAPE if cap is too small).
@@ -197,9 +209,10 @@ GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn
  *   stages   depth of the TMA -> MMA shared-memory ring
  *   grid     CTAs launched (persistent: one per SM, at most one per work item)
  *   colgroup, rowgroup  the schedule shape in effect (see gemm_rs_set_schedule)
+ *   reduce_mode         GEMM_RS_REDUCE_CHAIN or GEMM_RS_REDUCE_LAST_ARRIVER
  */
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
-                                 int *colgroup, int *rowgroup);
+                                 int *colgroup, int *rowgroup, int *reduce_mode);
 
 /* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
  * (bm = 128).  Returns ERR_ARG for any other value. */
@@ -225,6 +238,12 @@ GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
  *             capped at the chunk.  Smaller groups re-read B once per sweep.
  * Returns ERR_ARG for negative values. */
 GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup);
+
+/* Select the reduction (GEMM_RS_REDUCE_*).  Both give Y within the stated
+ * tolerances of each other.  Each is bit-identical from run to run.  They
+ * differ in summation order: rank order 0..W-1 for LAST_ARRIVER, the steps'
+ * order for CHAIN.  ERR_ARG for other values. */
+GEMM_RS_API int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode);
 
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
 

@@ -35,6 +35,9 @@ GEMM_RS_ERR_WORKSPACE = -7
 
 GEMM_RS_DEBUG_STALL_PRODUCER = 1
 
+GEMM_RS_REDUCE_CHAIN = 0
+GEMM_RS_REDUCE_LAST_ARRIVER = 1
+
 _DTYPES = {"bf16": GEMM_RS_BF16, "fp32": GEMM_RS_FP32}
 
 _lock = threading.Lock()
@@ -71,7 +74,8 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_status": (i32, [vp, vp]),
             "gemm_rs_reset": (i32, [vp, vp]),
             "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, i32, i32, vp, i64]),
-            "gemm_rs_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 6),
+            "gemm_rs_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 7),
+            "gemm_rs_set_reduce_mode": (i32, [vp, i32]),
             "gemm_rs_set_schedule": (i32, [vp, i32, i32]),
             "gemm_rs_set_tile_n": (i32, [vp, i32]),
             "gemm_rs_set_tile": (i32, [vp, i32, i32]),
@@ -146,10 +150,14 @@ def gemm_rs_schedule(M: int, N: int, W: int, bm: int, bn: int, colgroup: int = 0
 
 
 def gemm_rs_get_plan(h) -> dict:
-    v = [ctypes.c_int() for _ in range(6)]
+    v = [ctypes.c_int() for _ in range(7)]
     _check(lib().gemm_rs_get_plan(h, *[ctypes.byref(x) for x in v]))
-    return dict(zip(("bm", "bn", "stages", "grid", "colgroup", "rowgroup"),
+    return dict(zip(("bm", "bn", "stages", "grid", "colgroup", "rowgroup", "reduce_mode"),
                     (x.value for x in v)))
+
+
+def gemm_rs_set_reduce_mode(h, mode: int) -> None:
+    _check(lib().gemm_rs_set_reduce_mode(h, mode))
 
 
 def gemm_rs_set_schedule(h, colgroup: int = 0, rowgroup: int = 0) -> None:

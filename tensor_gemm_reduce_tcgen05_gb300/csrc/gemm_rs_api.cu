@@ -80,6 +80,8 @@ int check_shape(int64_t M, int64_t N, int64_t K, int W)
     if (N % 8 != 0)
         return fail(GEMM_RS_ERR_SHAPE, "N = %lld is not a multiple of 8 (16-byte rows)",
                     (long long)N);
+    if (cdiv(M, 128) * cdiv(N, 64) >= (int64_t(1) << 25))
+        return fail(GEMM_RS_ERR_SHAPE, "more than 2^25 output tiles");
     return GEMM_RS_OK;
 }
 
@@ -257,6 +259,7 @@ struct gemm_rs_s {
     int device, sms, pair_clusters, bm, bn;
     int colgroup; // 0: one group of all column tiles
     int rowgroup; // 0: the default (pick_rowgroup)
+    int reduce_mode; // GEMM_RS_REDUCE_CHAIN (default) or GEMM_RS_REDUCE_LAST_ARRIVER
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
     unsigned long long timeout;
@@ -328,6 +331,7 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     pick_tile(M, N, W, sms, &h->bm, &h->bn);
     h->colgroup = 0;
     h->rowgroup = 0;
+    h->reduce_mode = GEMM_RS_REDUCE_CHAIN;
     h->tmA_ptr = h->tmB_ptr = nullptr;
     h->timeout = 1ull << 32;
     h->record = nullptr;
@@ -343,7 +347,7 @@ int gemm_rs_destroy(gemm_rs_t h)
 }
 
 int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int *colgroup,
-                     int *rowgroup)
+                     int *rowgroup, int *reduce_mode)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
@@ -360,6 +364,8 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int 
     }
     if (rowgroup)
         *rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
+    if (reduce_mode)
+        *reduce_mode = h->reduce_mode;
     if (grid) {
         if (h->bm == 2 * gemm_rs::kBM) {
             const int64_t pairs = h->pair_clusters;
@@ -404,6 +410,16 @@ int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup)
                     rowgroup);
     h->colgroup = colgroup;
     h->rowgroup = rowgroup;
+    return GEMM_RS_OK;
+}
+
+int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (mode != GEMM_RS_REDUCE_CHAIN && mode != GEMM_RS_REDUCE_LAST_ARRIVER)
+        return fail(GEMM_RS_ERR_ARG, "unknown reduce mode %d", mode);
+    h->reduce_mode = mode;
     return GEMM_RS_OK;
 }
 
@@ -484,6 +500,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
     a.colgroup = (h->colgroup <= 0 || h->colgroup > a.nN) ? a.nN : h->colgroup;
     a.rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
+    a.chain = h->reduce_mode == GEMM_RS_REDUCE_CHAIN ? 1 : 0;
     a.R = h->M / h->W;
     a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
@@ -747,6 +764,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.nMs = a.nM;
     a.colgroup = a.nN;
     a.rowgroup = a.nM;
+    a.chain = 1;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

@@ -106,6 +106,7 @@ struct KernelArgs {
     int nMs;        // row tiles of the schedule (nM, or ceil(M/256) for CTA pairs)
     int colgroup;   // column tiles per schedule group (>= nN: one group)
     int rowgroup;   // row tiles per sweep (>= a chunk's row tiles: one sweep per step)
+    int chain;      // 1: chain reduction (in-order fold as tiles land), 0: last arriver reduces
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -130,6 +131,9 @@ struct SmemCtl {
     uint64_t drain;
     int32_t rq_tile[kRQ];
     uint32_t rq_head; // next queue entry to claim
+    int epi_direct[2]; // chain mode: the epilogue owns the fold of the tile in TMEM buffer b
+    int epi_fold;      // chain mode: position the epilogue folds on from (-1: none)
+    int epi_fold_end;  // chain mode: last stored position of the current fold
     uint32_t tmem_base;
     int abort;
 };
@@ -291,6 +295,28 @@ __device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Write 8 consecutive output columns (m, n .. n+7) of Y in its dtype.
+__device__ __forceinline__ void store_y8(const KernelArgs &a, int64_t m, int64_t n, float4 lo,
+                                         float4 hi)
+{
+    if (a.y_fp32) {
+        float *yp = static_cast<float *>(a.Y) + m * a.N + n;
+        ptx::st_f4(yp, lo);
+        ptx::st_f4(yp + 4, hi);
+    } else {
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(lo.x, lo.y);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(lo.z, lo.w);
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(hi.x, hi.y);
+        const __nv_bfloat162 h3 = __floats2bfloat162_rn(hi.z, hi.w);
+        uint4 w;
+        w.x = *reinterpret_cast<const uint32_t *>(&h0);
+        w.y = *reinterpret_cast<const uint32_t *>(&h1);
+        w.z = *reinterpret_cast<const uint32_t *>(&h2);
+        w.w = *reinterpret_cast<const uint32_t *>(&h3);
+        ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
+    }
+}
+
 // ------------------------------------------------------------------ reduce queue
 // Single producer (epilogue thread 0), several consumer warps.  An entry is
 // (tile << 2) | quarter, or -1 to stop one consumer.  Consumers claim entries
@@ -309,10 +335,14 @@ __device__ __forceinline__ bool rq_push(const KernelArgs &a, SmemCtl *ctl, uint3
     return true;
 }
 
-// One warp reduces one quarter (32 rows x BN columns) of an output tile: the
-// W partials are folded in rank order, converted, and written to Y.
+// y = slot[lo] + slot[lo+1] + ... + slot[hi], folded left to right in fp32,
+// for one quarter (32 rows x BN columns) of tile `tile`, by one warp (lane =
+// row).  to_y: convert and write Y.  Otherwise the sum is written back to
+// slot[hi] (a running sum).  The slots read (except a rewritten slot[hi]) are
+// dead afterwards, so their L2 lines are dropped without write-back.
 template <int BN>
-__device__ __forceinline__ void reduce_quarter(const KernelArgs &a, int tile, int q, int lane)
+__device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int q, int lane, int lo,
+                                             int hi, bool to_y)
 {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::kSlabs;
@@ -320,72 +350,107 @@ __device__ __forceinline__ void reduce_quarter(const KernelArgs &a, int tile, in
     const int nt = tile - mt * a.nN;
     const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
     const bool row_ok = m < a.M;
-    // rank 0's 32-row quarter; rank r's is kSlotFloats further on
-    const float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
-                      static_cast<int64_t>(q) * S * 1024;
+    // slot 0's 32-row quarter; slot s's is s * kSlotFloats further on
+    float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
+                static_cast<int64_t>(q) * S * 1024;
+    const int n_in = hi - lo + 1;
 #pragma unroll 1
     for (int slab = 0; slab < S; ++slab) {
-        const float *sb = qb + slab * 1024 + lane * 4;
+        const float *sb = qb + static_cast<int64_t>(lo) * Cfg::kSlotFloats + slab * 1024 + lane * 4;
+        float4 prev_half = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-        for (int jq = 0; jq < 4; ++jq) {
-            // float4 j = 2*jq and 2*jq+1: columns 8*jq .. 8*jq+7 of the slab.
-            float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-            for (int r0 = 0; r0 < a.W; r0 += 8) {
-                float4 u0[8], u1[8];
+        for (int jf = 0; jf < 8; ++jf) {
+            // float4 j = jf: columns 4*jf .. 4*jf+3 of the slab.
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < n_in; s0 += 8) {
+                float4 u[8];
+#pragma unroll
+                for (int uu = 0; uu < 8; ++uu)
+                    if (s0 + uu < n_in)
+                        u[uu] = ptx::ld_cg_f4(sb + static_cast<int64_t>(s0 + uu) * Cfg::kSlotFloats +
+                                              jf * 128);
+                // Fixed order: y = slot[lo], then y = y + slot[s].
 #pragma unroll
                 for (int uu = 0; uu < 8; ++uu) {
-                    if (r0 + uu < a.W) {
-                        const float *pp = sb + static_cast<int64_t>(r0 + uu) * Cfg::kSlotFloats +
-                                          (2 * jq) * 128;
-                        u0[uu] = ptx::ld_cg_f4(pp);
-                        u1[uu] = ptx::ld_cg_f4(pp + 128);
-                    }
-                }
-                // Fixed rank order: y = p_0, then y = y + p_r.
-#pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    if (r0 + uu < a.W) {
-                        if (r0 + uu == 0) {
-                            y0 = u0[uu];
-                            y1 = u1[uu];
+                    if (s0 + uu < n_in) {
+                        if (s0 + uu == 0) {
+                            y = u[uu];
                         } else {
-                            y0.x += u0[uu].x; y0.y += u0[uu].y; y0.z += u0[uu].z; y0.w += u0[uu].w;
-                            y1.x += u1[uu].x; y1.y += u1[uu].y; y1.z += u1[uu].z; y1.w += u1[uu].w;
+                            y.x += u[uu].x; y.y += u[uu].y; y.z += u[uu].z; y.w += u[uu].w;
                         }
                     }
                 }
             }
-            const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + jq * 8;
-            if (row_ok && n < a.N) { // N is a multiple of 8
-                if (a.y_fp32) {
-                    float *yp = static_cast<float *>(a.Y) + m * a.N + n;
-                    ptx::st_f4(yp, y0);
-                    ptx::st_f4(yp + 4, y1);
+            if (to_y) {
+                // Y is written 8 columns at a time: keep the even float4 until
+                // its odd neighbour is done.
+                if ((jf & 1) == 0) {
+                    prev_half = y;
                 } else {
-                    const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0.x, y0.y);
-                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(y0.z, y0.w);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(y1.x, y1.y);
-                    const __nv_bfloat162 h3 = __floats2bfloat162_rn(y1.z, y1.w);
-                    uint4 w;
-                    w.x = *reinterpret_cast<const uint32_t *>(&h0);
-                    w.y = *reinterpret_cast<const uint32_t *>(&h1);
-                    w.z = *reinterpret_cast<const uint32_t *>(&h2);
-                    w.w = *reinterpret_cast<const uint32_t *>(&h3);
-                    ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
+                    const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + (jf - 1) * 4;
+                    if (row_ok && n < a.N) // N is a multiple of 8
+                        store_y8(a, m, n, prev_half, y);
                 }
+            } else {
+                ptx::st_f4(qb + static_cast<int64_t>(hi) * Cfg::kSlotFloats + slab * 1024 + lane * 4 +
+                               jf * 128,
+                           y);
             }
         }
-        // Every lane has read this slab of every rank.  The partials are dead
-        // until the next call rewrites them, so drop their L2 lines without
-        // write-back (lane l drops line l of each 4 KB block).
+        // Every lane has read this slab of every slot: drop the dead lines
+        // (lane l drops line l of each 4 KB block).
         __syncwarp();
-        for (int r = 0; r < a.W; ++r)
-            ptx::discard_l2_line(qb + static_cast<int64_t>(r) * Cfg::kSlotFloats + slab * 1024 +
+        const int last_dead = to_y ? hi : hi - 1;
+        for (int s = lo; s <= last_dead; ++s)
+            ptx::discard_l2_line(qb + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 +
                                  lane * 32);
     }
 }
 
-// A consumer warp: claim entries until it takes a stop entry.
+// ---------------------------------------------------------------- chain reduction state
+// In the chain mode each output tile has one 32-bit state word:
+//   bits  0-15  positions whose partial is stored in their slot and not yet folded
+//   bits 16-20  k: positions 0 .. k-1 are folded; their running sum is in slot k-1
+//   bit  24     owned: one CTA is folding from position k on
+// Position i is the step in which its rank reaches the tile, so in a steady run
+// the positions arrive in order and each one folds itself straight from TMEM.
+constexpr uint32_t kChainOwn = 1u << 24;
+__device__ __forceinline__ uint32_t chain_k(uint32_t s) { return (s >> 16) & 31u; }
+
+// Take the fold at position i: true if positions 0 .. i-1 are folded, nobody
+// owns the tile, and the caller now owns it.
+__device__ __forceinline__ bool chain_try_own(uint32_t *flag, uint32_t i)
+{
+    uint32_t s = ptx::ld_acquire_gpu(flag);
+    while (chain_k(s) == i && !(s & kChainOwn)) {
+        const uint32_t prev = ptx::atom_cas_acq_rel_gpu(flag, s, s | kChainOwn);
+        if (prev == s)
+            return true;
+        s = prev;
+    }
+    return false;
+}
+
+// The owner has folded positions 0 .. kn-1 (running sum in slot kn-1).  If
+// position kn is already stored, it keeps the ownership and returns true (the
+// caller folds on from kn).  Otherwise it publishes k = kn and releases.
+__device__ __forceinline__ bool chain_pass_on(uint32_t *flag, uint32_t kn)
+{
+    uint32_t s = ptx::ld_acquire_gpu(flag);
+    while (true) {
+        if ((s >> kn) & 1u)
+            return true;
+        const uint32_t nv = (kn << 16) | ((s & 0xFFFFu) & ~((1u << kn) - 1u));
+        const uint32_t prev = ptx::atom_cas_acq_rel_gpu(flag, s, nv);
+        if (prev == s)
+            return false;
+        s = prev;
+    }
+}
+
+// A consumer warp: claim entries until it takes a stop entry.  Entry kinds:
+//   (tile << 2) | q   last-arriver mode: fold all W slots of quarter q into Y
+//   -1                stop
 template <int BN>
 __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, int lane)
 {
@@ -412,7 +477,7 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
         }
         if (entry < 0)
             break;
-        reduce_quarter<BN>(a, entry >> 2, entry & 3, lane);
+        fold_quarter<BN>(a, entry >> 2, entry & 3, lane, 0, a.W - 1, true);
     }
 }
 
@@ -420,6 +485,16 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
 // PAIR: the CTA is half `crank` of a 256-row pair tile.  It drains its own
 // TMEM, waits with cluster-scope acquire, and hands the accumulator back to
 // the pair's MMA thread (in CTA 0).
+//
+// Last-arriver mode: every rank stores its partial in slot r, counts itself in
+// on the tile's counter, and the rank that arrives last queues the tile: the
+// consumers fold slots 0 .. W-1 (rank order) into Y.
+// Chain mode: the rank at position i (its step) folds its own partial straight
+// from TMEM onto the running sum in slot i-1 when positions 0 .. i-1 are done,
+// writing slot i, or Y at the last position.  A rank that is early stores its
+// partial in slot i.  Whoever owns the fold when the positions after it are
+// already stored (or the early rank itself, once its turn has come) folds
+// them from their slots with all four epilogue warps, one quarter each.
 template <int BN, bool PAIR>
 __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &sch, uint32_t tmem,
                                              SmemCtl *ctl, int warp, int lane, int64_t g0,
@@ -430,18 +505,25 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     const int q = warp & 3;                           // TMEM lanes [32q, 32q + 32)
     const int etid = threadIdx.x - kEpiWarp0 * 32;    // 0 .. 127
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    // Partials are read back only at the end of the schedule: do not let them
-    // push the B panels out of L2.
-    const uint64_t st_pol = ptx::policy_evict_first();
+    // Last-arriver partials are read back only at the end of the schedule: do
+    // not let them push the B panels out of L2.  Chain-mode slots are read at
+    // the next step: keep them.
+    const uint64_t st_pol = a.chain ? ptx::policy_evict_normal() : ptx::policy_evict_first();
     bool ok = true;
     uint32_t rq_n = 0;
     int it = 0;
     for (int64_t g = g0; g < a.total; g += gstride, ++it) {
-        int r, mts, nt;
-        decode_tile(sch, g, r, mts, nt);
+        int r, mts, nt, step;
+        decode_tile(sch, g, r, mts, nt, step);
         const int mt = PAIR ? 2 * mts + static_cast<int>(crank) : mts;
         const bool half_ok = mt < a.nM; // a pair's second half may lie wholly below M
+        const int tile = mt * a.nN + nt;
         const int buf = it & 1;
+        // Chain mode: try to take the fold while the accumulator is still being
+        // computed, so the decision is ready when it lands.
+        if (etid == 0)
+            ctl->epi_direct[buf] =
+                (a.chain && half_ok && chain_try_own(a.flags + tile, static_cast<uint32_t>(step))) ? 1 : 0;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
         const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
@@ -462,13 +544,33 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             }
             continue;
         }
+        const bool direct = *reinterpret_cast<volatile int *>(&ctl->epi_direct[buf]) != 0;
+        const int sidx = a.chain ? step : r;                 // slot written
+        const bool to_y = direct && step == a.W - 1;         // the last fold writes Y
+        const bool add_prev = direct && step > 0;            // fold onto slot step-1
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
-        float *slot = a.part + ((static_cast<int64_t>(mt) * a.nN + nt) * a.W + r) * Cfg::kSlotFloats +
-                      static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
+        float *tb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
+                    static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
+        float *slot = tb + static_cast<int64_t>(sidx) * Cfg::kSlotFloats;
+        const float *prev = tb + static_cast<int64_t>(step > 0 ? step - 1 : 0) * Cfg::kSlotFloats;
+        // The running sum of slot step-1 is loaded one slab ahead, so its
+        // latency overlaps the previous slab's work.
+        float4 rs[8];
+        if (add_prev) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                rs[j] = ptx::ld_cg_f4(prev + j * 128);
+        }
 #pragma unroll 1
         for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
+            float4 rn[8];
+            if (add_prev && slab + 1 < Cfg::kSlabs) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    rn[j] = ptx::ld_cg_f4(prev + (slab + 1) * 1024 + j * 128);
+            }
             uint32_t v[32];
             if (a.nK > 0) {
                 ptx::tmem_ld_32x32b_x32(tmem + lane_base + static_cast<uint32_t>(buf * BN + slab * 32),
@@ -510,27 +612,104 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     }
                 }
             }
-            float *dst = slot + slab * 1024;
+            if (add_prev) {
+                // running sum first, then this position's partial
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                ptx::st_f4_hint(dst + j * 128,
-                                make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]), st_pol);
+                for (int j = 0; j < 8; ++j) {
+                    p[4 * j] = rs[j].x + p[4 * j];
+                    p[4 * j + 1] = rs[j].y + p[4 * j + 1];
+                    p[4 * j + 2] = rs[j].z + p[4 * j + 2];
+                    p[4 * j + 3] = rs[j].w + p[4 * j + 3];
+                }
+            }
+            if (to_y) {
+                const int64_t n0 = static_cast<int64_t>(nt) * BN + slab * 32;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    const int64_t n = n0 + 8 * g8;
+                    if (row_ok && n < a.N)
+                        store_y8(a, m, n,
+                                 make_float4(p[8 * g8], p[8 * g8 + 1], p[8 * g8 + 2], p[8 * g8 + 3]),
+                                 make_float4(p[8 * g8 + 4], p[8 * g8 + 5], p[8 * g8 + 6], p[8 * g8 + 7]));
+                }
+            } else {
+                float *dst = slot + slab * 1024;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ptx::st_f4_hint(dst + j * 128,
+                                    make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]),
+                                    st_pol);
+            }
+            if (add_prev) {
+                // slot step-1 is dead: drop its lines of this warp's 4 KB block
+                __syncwarp();
+                ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    rs[j] = rn[j];
+            }
         }
 
         // Every epilogue thread has issued its stores.  Publish them at gpu
-        // scope and count this rank in.
+        // scope, then take the tile's next step.
         ptx::named_bar_sync(kBarEpi, 128);
         if (etid == 0) {
             __threadfence();
-            uint32_t *flag = a.flags + static_cast<int64_t>(mt) * a.nN + nt;
-            const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
-            if (old == static_cast<uint32_t>(a.W - 1)) {
-                // Last arriver: the counter goes back to 0 for the next call
-                // (no memset), and the tile goes to the reducers.
-                ptx::st_relaxed_gpu(flag, 0u);
-                const int32_t tile = mt * a.nN + nt;
-                for (int qq = 0; qq < 4 && ok; ++qq)
-                    ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
+            uint32_t *flag = a.flags + tile;
+            if (!a.chain) {
+                const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
+                if (old == static_cast<uint32_t>(a.W - 1)) {
+                    // Last arriver: the counter goes back to 0 for the next call
+                    // (no memset), and the tile goes to the reducers.
+                    ptx::st_relaxed_gpu(flag, 0u);
+                    for (int qq = 0; qq < 4 && ok; ++qq)
+                        ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
+                }
+            } else {
+                int fold_from = -1;
+                if (direct) {
+                    if (to_y)
+                        ptx::st_relaxed_gpu(flag, 0u); // back to 0 for the next call
+                    else if (chain_pass_on(flag, static_cast<uint32_t>(step + 1)))
+                        fold_from = step + 1;
+                } else {
+                    const uint32_t old = ptx::atom_or_acq_rel_gpu(flag, 1u << step);
+                    if (chain_k(old) == static_cast<uint32_t>(step) && !(old & kChainOwn) &&
+                        chain_try_own(flag, static_cast<uint32_t>(step)))
+                        fold_from = step;
+                }
+                ctl->epi_fold = fold_from;
+            }
+        }
+        if (a.chain) {
+            // Fold on while the positions after the running sum are already
+            // stored: every warp takes its own quarter of the tile.
+            ptx::named_bar_sync(kBarEpi, 128);
+            int k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
+            while (k >= 0) {
+                uint32_t *flag = a.flags + tile;
+                if (etid == 0) {
+                    const uint32_t st = ptx::ld_acquire_gpu(flag);
+                    int j = k;
+                    while (j + 1 < a.W && ((st >> (j + 1)) & 1u))
+                        ++j;
+                    ctl->epi_fold_end = j;
+                }
+                ptx::named_bar_sync(kBarEpi, 128);
+                const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
+                fold_quarter<BN>(a, tile, q, lane, k > 0 ? k - 1 : k, j, j == a.W - 1);
+                ptx::named_bar_sync(kBarEpi, 128);
+                if (etid == 0) {
+                    __threadfence();
+                    int next = -1;
+                    if (j == a.W - 1)
+                        ptx::st_relaxed_gpu(flag, 0u);
+                    else if (chain_pass_on(flag, static_cast<uint32_t>(j + 1)))
+                        next = j + 1;
+                    ctl->epi_fold = next;
+                }
+                ptx::named_bar_sync(kBarEpi, 128);
+                k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
             }
         }
     }

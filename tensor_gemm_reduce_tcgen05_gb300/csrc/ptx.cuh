@@ -363,6 +363,32 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+__device__ __forceinline__ uint32_t atom_or_acq_rel_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.or.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Compare-and-swap; returns the value found.
+__device__ __forceinline__ uint32_t atom_cas_acq_rel_gpu(uint32_t *p, uint32_t expect, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(old)
+                 : "l"(p), "r"(expect), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -14,15 +14,15 @@
 //     for each step s = 0 .. W-1 (chunk (r+1+s) mod W):
 //       for each row group of the chunk (RG row tiles; one group when RG
 //       covers the chunk):
-//         one sweep over the column tiles of the column group, forward on
-//         even sweeps and backward on odd ones (sweeps counted from the start
-//         of the column group), so that the B columns used last are the
-//         first used again;
+//         one sweep over the column tiles of the column group,
 //           for each row tile of the row group, ascending.
-// Column tiles are counted from offset (r*nN)/W.  Row groups bound the A rows
+// Column tiles are counted from offset ((W-r) mod W)*nN/W.  Row groups bound the A rows
 // a sweep keeps live, so they can stay in L2 while the columns go by.  The
 // ranks advance side by side: global entry g is rank (g mod W)'s (g / W)-th
-// tile.
+// tile.  Every sweep runs forward, and the rank that reaches a tile at step
+// s+1 (rank r-1) starts its sweep nN/W columns earlier than rank r: it
+// reaches the tile between 1 - 1/W and about 2 steps after rank r did, so a
+// tile's contributions arrive in step order.
 #pragma once
 
 #include <cstdint>
@@ -43,20 +43,20 @@ __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
     return (x + (int64_t(1) << s) - 1) >> s;
 }
 
-// Decode global entry g into (r, mt, nt).  g must be < W*nM*nN.
+// Decode global entry g into (r, mt, nt) and the step (0 .. W-1) in which rank
+// r reaches the tile's chunk.  g must be < W*nM*nN.
 __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
-                                                     int &nt)
+                                                     int &nt, int &step)
 {
     r = static_cast<int>(g % s.W);
     int64_t p = g / s.W;
-    const int64_t rot = (static_cast<int64_t>(r) * s.nN) / s.W;
+    const int64_t rot = (static_cast<int64_t>((s.W - r) % s.W) * s.nN) / s.W;
     const int64_t G = s.G < s.nN ? s.G : s.nN;
     // Every group but the last is full, so the group index follows directly.
     const int64_t grp = p / (G * s.nM);
     p -= grp * G * s.nM;
     const int64_t g0 = grp * G;
     const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
-    int64_t sweep = 0; // column sweeps before the current step
     for (int st = 0; st < s.W; ++st) {
         int c = r + 1 + st;
         if (c >= s.W)
@@ -76,19 +76,25 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
             const int64_t rn = (cnt - rg * RG) < RG ? (cnt - rg * RG) : RG;
             const int64_t jl = q / rn;
             mt = static_cast<int>(first + rg * RG + (q - jl * rn));
-            const int64_t j = ((sweep + rg) & 1) ? gn - 1 - jl : jl;
-            int64_t n = g0 + j + rot;
+            int64_t n = g0 + jl + rot;
             if (n >= s.nN)
                 n -= s.nN;
             nt = static_cast<int>(n);
+            step = st;
             return;
         }
         p -= items;
-        if (cnt > 0)
-            sweep += (cnt + RG - 1) / RG;
     }
     mt = -1;
     nt = -1;
+    step = -1;
+}
+
+__host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
+                                                     int &nt)
+{
+    int step;
+    decode_tile(s, g, r, mt, nt, step);
 }
 
 } // namespace gemm_rs

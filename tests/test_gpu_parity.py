@@ -31,13 +31,18 @@ SHAPES = [
 TILES = [(128, 256), (128, 128), (128, 64), (256, 256)]  # (256, 256): the CTA-pair kernel
 
 
+MODES = [0, 1]  # GEMM_RS_REDUCE_CHAIN, GEMM_RS_REDUCE_LAST_ARRIVER
+
+
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
-def test_integer_inputs_bit_exact(W, M, N, Kpr, tile):
+def test_integer_inputs_bit_exact(W, M, N, Kpr, tile, mode):
     A, B, _ = inputs(W, M, N, Kpr, "int")
-    y, plan, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
-                         tile_n=tile[1])
-    assert (plan["bm"], plan["bn"]) == tile
+    y, plan, op = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
+                          tile_n=tile[1], reduce_mode=mode)
+    assert (plan["bm"], plan["bn"], plan["reduce_mode"]) == (tile[0], tile[1], mode)
+    assert int(op.flags_view().abs().sum()) == 0
     ref = oracle_y(A, B, None, 1.0, 0.0, "fp32")
     np.testing.assert_array_equal(y, ref)
 
@@ -53,11 +58,12 @@ def test_integer_inputs_with_c_bit_exact(W, M, N, Kpr, tile):
         np.testing.assert_array_equal(y, ref)
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
 @pytest.mark.parametrize("y_dtype", ["fp32", "bf16"])
-def test_normal_inputs_within_tolerance(W, M, N, Kpr, y_dtype):
+def test_normal_inputs_within_tolerance(W, M, N, Kpr, y_dtype, mode):
     A, B, C = inputs(W, M, N, Kpr, "normal", c_dist="normal1")
-    y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype)
+    y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype, reduce_mode=mode)
     assert_close(y, oracle_y(A, B, C, 0.5, 1.0, y_dtype), y_dtype, f"{(W, M, N, Kpr)}")
 
 
@@ -74,8 +80,9 @@ def test_nan_poisoned_workspace_and_output():
     W, M, N, Kpr = 3, 300, 520, 200
     A, B, _ = inputs(W, M, N, Kpr, "int")
     for tile in ((128, 256), (128, 64), (256, 256)):
-        y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
-                          tile_n=tile[1], poison=True)
+        for mode in MODES:
+            y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
+                              tile_n=tile[1], poison=True, reduce_mode=mode)
         np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
@@ -109,13 +116,15 @@ def test_empty_problem_is_a_no_op():
     assert op.status() == 0
 
 
-def test_twenty_calls_bit_identical_and_counters_reset():
+@pytest.mark.parametrize("mode", MODES)
+def test_twenty_calls_bit_identical_and_counters_reset(mode):
     """Workspace reused across back-to-back calls with no memset: identical
     results every call, and every tile counter is 0 afterwards."""
     W, M, N, Kpr = 4, 1024, 640, 256
     A, B, _ = inputs(W, M, N, Kpr, "uniform")
-    from tensor_gemm_reduce_tcgen05_gb300.binding import GemmRS
-    op = GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    b.gemm_rs_set_reduce_mode(op.handle, mode)
     Ad, Bd = A.cuda(), B.cuda()
     outs = [op.run(Ad, Bd) for _ in range(20)]
     torch.cuda.synchronize()
@@ -182,6 +191,22 @@ def test_timeout_path_reports_and_recovers(tile):
     np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
+def test_reduce_modes_agree_and_each_is_deterministic():
+    """Both reductions on one shape with many tiles per chunk: each is bit-identical
+    across calls, and the two agree within the fp32 tolerance (they differ only in
+    summation order)."""
+    W, M, N, Kpr = 8, 2048, 1536, 512
+    A, B, _ = inputs(W, M, N, Kpr, "normal")
+    outs = {}
+    for mode in MODES:
+        y1, _, op = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode, calls=3)
+        y2, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode)
+        np.testing.assert_array_equal(y1, y2)
+        outs[mode] = y1
+    assert_close(outs[0], outs[1], "fp32", "chain vs last arriver")
+    assert_close(outs[0], oracle_y(A, B, None, 1.0, 0.0, "fp32"), "fp32", "chain vs oracle")
+
+
 def test_baseline_reduce_kernel_matches_oracle():
     """The unfused baseline's separate reduce step, given exact per-rank
     partials, reproduces the oracle's fold."""
@@ -199,9 +224,10 @@ def test_baseline_reduce_kernel_matches_oracle():
         np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, C, 0.5, 1.0, y_dtype))
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["ffn_w8_m4096", "ffn_w8_m8192_bias", "decode_w8_m64",
                                   "ffn_w4_m16384_x20"])
-def test_full_size_workloads_on_row_sample(name):
+def test_full_size_workloads_on_row_sample(name, mode):
     """The full-size workloads in the launch configuration the benchmark
     times, checked on a row sample: every chunk's first and last row, four
     row-tile boundaries (both rows at each), and 8 seeded random rows.  The
@@ -209,7 +235,7 @@ def test_full_size_workloads_on_row_sample(name):
     w = WORKLOADS[name]
     A, B, C = workload_inputs(w)
     y, plan, op = run_gpu(A, B, C, w.W, w.M, w.N, w.Kpr, w.alpha, w.beta, w.y_dtype,
-                          calls=w.calls)
+                          calls=w.calls, reduce_mode=mode)
     rows = sample_rows(w.M, w.W, n_random=8, n_boundaries=4)
     ref = oracle_y(A, B, C, w.alpha, w.beta, w.y_dtype, rows=rows)
     assert_close(y[rows], ref, w.y_dtype, name)

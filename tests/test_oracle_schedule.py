@@ -86,51 +86,67 @@ def test_schedule_properties(W, M, N, BM, BN, G, RG):
             assert len(chunks) == W
 
 
-def test_serpentine_column_order_between_steps():
-    """Consecutive steps walk the column tiles in opposite directions, so a
-    rank's last column tile of one step is its first of the next."""
+def test_every_sweep_runs_forward_from_the_rank_offset():
+    """Each step sweeps a rank's column tiles forward from ((W-r) mod W)*nN/W."""
     W, M, N, BM, BN = 4, 4 * 128, 2048, 128, 256
     sched = oracle.schedule(W, M, N, BM, BN)
     nN = N // BN
     for r in range(W):
         cols = [int(nt) for (rr, mt, nt) in sched if rr == r]
-        steps = [cols[s * nN:(s + 1) * nN] for s in range(W)]
-        rot = (r * nN) // W
-        assert steps[0] == [(j + rot) % nN for j in range(nN)]
-        for s in range(1, W):
-            assert steps[s] == steps[s - 1][::-1]
+        rot = (((W - r) % W) * nN) // W
+        for s in range(W):
+            assert cols[s * nN:(s + 1) * nN] == [(j + rot) % nN for j in range(nN)]
 
 
 def test_row_groups_sweep_all_columns_per_group():
     """With row groups of 2 row tiles, a step of a 6-tile chunk makes three
-    sweeps over the column tiles, alternating direction, each covering its
-    two row tiles for every column."""
+    forward sweeps over the column tiles, each covering its two row tiles for
+    every column."""
     W, M, N, BM, BN, RG = 2, 2 * 6 * 128, 1024, 128, 256, 2
     sched = oracle.schedule(W, M, N, BM, BN, 0, RG)
     nN = N // BN
     mine = [(int(mt), int(nt)) for (rr, mt, nt) in sched if rr == 0]
     step0 = mine[:6 * nN]              # rank 0, step 0: chunk 1 (row tiles 6..11)
-    rot = 0
+    rot = (W * nN // W) % nN  # rank 0: offset ((W-0) mod W)*nN/W = 0
     for k in range(3):
         sweep = step0[k * 2 * nN:(k + 1) * 2 * nN]
         cols = [sweep[2 * i][1] for i in range(nN)]
-        fwd = [(j + rot) % nN for j in range(nN)]
-        assert cols == (fwd if k % 2 == 0 else fwd[::-1])
+        assert cols == [(j + rot) % nN for j in range(nN)]
         for i in range(nN):
             assert [sweep[2 * i][0], sweep[2 * i + 1][0]] == [6 + 2 * k, 7 + 2 * k]
 
 
+def test_tile_contributions_arrive_in_step_order():
+    """For every output tile, the global order visits its W rank contributions
+    in step order, each at least (1 - 1/W) of a step after the previous one.
+    The chain reduction folds them in that order."""
+    for (W, M, N, BM, BN) in [(8, 4096, 4096, 256, 256), (4, 16384, 5120, 256, 256),
+                              (8, 8192, 8192, 256, 256), (2, 1024, 2048, 128, 256)]:
+        sched = oracle.schedule(W, M, N, BM, BN)
+        nM, nN = -(-M // BM), -(-N // BN)
+        per_step = (W * nM * nN) // W  # global entries per step (equal chunk sizes here)
+        R = M // W
+        seen = {}
+        for g, (r, mt, nt) in enumerate(sched.tolist()):
+            seen.setdefault((mt, nt), []).append((g, r))
+        for (mt, nt), lst in seen.items():
+            c = (mt * BM) // R
+            steps = [((c - r - 1) % W) for (_, r) in lst]
+            assert steps == list(range(W))               # arrival order = step order
+            gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
+            assert min(gaps) >= per_step * (W - 1) // W - W  # ranks interleave: -1 per rank
+
+
 def test_rank_column_offset_when_one_chunk_holds_all_tiles():
     """M = 64, W = 8: chunks of 8 rows, one row tile (keyed to chunk 0).  Rank
-    r reaches chunk 0 at step s = W-1-r.  It starts at column (r*nN)/W, or
-    walks backwards from the column before it when s is odd, so the ranks
-    start on different column tiles."""
+    r reaches chunk 0 at step s = W-1-r and sweeps forward from column
+    ((W-r) mod W)*nN/W, so the ranks start on different column tiles."""
     W, M, N, BM, BN = 8, 64, 8192, 128, 64
     sched = oracle.schedule(W, M, N, BM, BN)
     nN = N // BN
     first = sched[:W]
     expect = []
     for r in range(W):
-        expect.append((r * nN) // W)  # one sweep per rank, forward
+        expect.append((((W - r) % W) * nN) // W)  # one sweep per rank, forward
     assert first[:, 2].tolist() == expect
     assert len(set(expect)) == W
