@@ -182,9 +182,10 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
  *  - A tile belongs to the chunk of its first row: key(mt) = (mt*BM) / R.
  *  - Rank r visits chunks in the order (r+1+s) mod W for s = 0 .. W-1, so its
  *    own chunk r comes last.
- *  - The column tiles, counted from offset ((W-r) mod W)*nN/W, form groups of G tiles
- *    (G <= 0 or G >= nN: a single group).  For each group, in order, the rank
- *    runs all W steps.  In a step, the chunk's row tiles (ascending) are split
+ *  - The column tiles form groups of G consecutive tiles (G <= 0 or G >= nN: a
+ *    single group).  For each group, in order, the rank runs all W steps.
+ *    Inside a group of gn tiles the rank starts at the group's tile
+ *    ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the chunk's row tiles (ascending) are split
  *    into row groups of RG tiles (RG <= 0: the whole chunk).  Each row group is
  *    one forward sweep over the group's column tiles.  For each column tile a
  *    sweep takes the row group's tiles in ascending order.
@@ -214,9 +215,9 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int 
     const int64_t group = (G <= 0 || G >= nN) ? nN : G;
     for (int r = 0; r < W; ++r) {
         int64_t p = 0;
-        const int64_t rot = ((int64_t)((W - r) % W) * nN) / W;
         for (int64_t g0 = 0; g0 < nN; g0 += group) {
             const int64_t gn = (nN - g0 < group) ? nN - g0 : group;
+            const int64_t rot = ((int64_t)((W - r) % W) * gn) / W;
             for (int s = 0; s < W; ++s) {
                 const int64_t c = (r + 1 + s) % W;
                 /* the chunk's row tiles, ascending */
@@ -228,7 +229,7 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int 
                 for (int64_t r0 = 0; r0 < n_rows; r0 += rgs) {
                     const int64_t r1 = (r0 + rgs < n_rows) ? r0 + rgs : n_rows;
                     for (int64_t j = 0; j < gn; ++j) {
-                        const int64_t nt = (g0 + j + rot) % nN;
+                        const int64_t nt = g0 + (j + rot) % gn;
                         for (int64_t i = r0; i < r1; ++i) {
                             list[2 * p] = (int32_t)rows[i];
                             list[2 * p + 1] = (int32_t)nt;

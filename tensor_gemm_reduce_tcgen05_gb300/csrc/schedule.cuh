@@ -16,13 +16,15 @@
 //       covers the chunk):
 //         one sweep over the column tiles of the column group,
 //           for each row tile of the row group, ascending.
-// Column tiles are counted from offset ((W-r) mod W)*nN/W.  Row groups bound the A rows
-// a sweep keeps live, so they can stay in L2 while the columns go by.  The
-// ranks advance side by side: global entry g is rank (g mod W)'s (g / W)-th
-// tile.  Every sweep runs forward, and the rank that reaches a tile at step
-// s+1 (rank r-1) starts its sweep nN/W columns earlier than rank r: it
-// reaches the tile between 1 - 1/W and about 2 steps after rank r did, so a
-// tile's contributions arrive in step order.
+// Inside a column group of gn tiles, rank r's sweep starts at the group's tile
+// ((W-r) mod W)*gn/W and wraps around within the group, so all ranks cover
+// the same columns in a group and each B panel of the group stays in use for
+// all W steps.  Row groups bound the A rows a sweep keeps live, so they can
+// stay in L2 while the columns go by.  The ranks advance side by side: global
+// entry g is rank (g mod W)'s (g / W)-th tile.  Every sweep runs forward, and
+// the rank that reaches a tile at step s+1 (rank r-1) starts its sweep gn/W
+// columns earlier than rank r: it reaches the tile between 1 - 1/W and about
+// 2 steps after rank r did, so a tile's contributions arrive in step order.
 #pragma once
 
 #include <cstdint>
@@ -50,13 +52,13 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
 {
     r = static_cast<int>(g % s.W);
     int64_t p = g / s.W;
-    const int64_t rot = (static_cast<int64_t>((s.W - r) % s.W) * s.nN) / s.W;
     const int64_t G = s.G < s.nN ? s.G : s.nN;
     // Every group but the last is full, so the group index follows directly.
     const int64_t grp = p / (G * s.nM);
     p -= grp * G * s.nM;
     const int64_t g0 = grp * G;
     const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
+    const int64_t rot = (static_cast<int64_t>((s.W - r) % s.W) * gn) / s.W;
     for (int st = 0; st < s.W; ++st) {
         int c = r + 1 + st;
         if (c >= s.W)
@@ -76,10 +78,10 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
             const int64_t rn = (cnt - rg * RG) < RG ? (cnt - rg * RG) : RG;
             const int64_t jl = q / rn;
             mt = static_cast<int>(first + rg * RG + (q - jl * rn));
-            int64_t n = g0 + jl + rot;
-            if (n >= s.nN)
-                n -= s.nN;
-            nt = static_cast<int>(n);
+            int64_t n = jl + rot;
+            if (n >= gn)
+                n -= gn;
+            nt = static_cast<int>(g0 + n);
             step = st;
             return;
         }

@@ -87,7 +87,8 @@ def test_schedule_properties(W, M, N, BM, BN, G, RG):
 
 
 def test_every_sweep_runs_forward_from_the_rank_offset():
-    """Each step sweeps a rank's column tiles forward from ((W-r) mod W)*nN/W."""
+    """Each step sweeps a rank's column tiles forward from ((W-r) mod W)*nN/W
+    (one column group)."""
     W, M, N, BM, BN = 4, 4 * 128, 2048, 128, 256
     sched = oracle.schedule(W, M, N, BM, BN)
     nN = N // BN
@@ -116,25 +117,30 @@ def test_row_groups_sweep_all_columns_per_group():
             assert [sweep[2 * i][0], sweep[2 * i + 1][0]] == [6 + 2 * k, 7 + 2 * k]
 
 
-def test_tile_contributions_arrive_in_step_order():
+@pytest.mark.parametrize("W,M,N,BM,BN,G", [
+    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
+    (2, 1024, 2048, 128, 256, 0), (8, 4096, 4096, 256, 256, 8), (8, 8192, 8192, 256, 256, 16),
+    (4, 16384, 5120, 256, 256, 8)])
+def test_tile_contributions_arrive_in_step_order(W, M, N, BM, BN, G):
     """For every output tile, the global order visits its W rank contributions
-    in step order, each at least (1 - 1/W) of a step after the previous one.
-    The chain reduction folds them in that order."""
-    for (W, M, N, BM, BN) in [(8, 4096, 4096, 256, 256), (4, 16384, 5120, 256, 256),
-                              (8, 8192, 8192, 256, 256), (2, 1024, 2048, 128, 256)]:
-        sched = oracle.schedule(W, M, N, BM, BN)
-        nM, nN = -(-M // BM), -(-N // BN)
-        per_step = (W * nM * nN) // W  # global entries per step (equal chunk sizes here)
-        R = M // W
-        seen = {}
-        for g, (r, mt, nt) in enumerate(sched.tolist()):
-            seen.setdefault((mt, nt), []).append((g, r))
-        for (mt, nt), lst in seen.items():
-            c = (mt * BM) // R
-            steps = [((c - r - 1) % W) for (_, r) in lst]
-            assert steps == list(range(W))               # arrival order = step order
-            gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
-            assert min(gaps) >= per_step * (W - 1) // W - W  # ranks interleave: -1 per rank
+    in step order, each at least (1 - 1/W) of a step after the previous one,
+    also with column groups (a step then covers one group's columns).  The
+    chain reduction folds them in that order."""
+    sched = oracle.schedule(W, M, N, BM, BN, G)
+    nM, nN = -(-M // BM), -(-N // BN)
+    group = nN if G <= 0 or G >= nN else G
+    R = M // W
+    seen = {}
+    for g, (r, mt, nt) in enumerate(sched.tolist()):
+        seen.setdefault((mt, nt), []).append((g, r))
+    for (mt, nt), lst in seen.items():
+        c = (mt * BM) // R
+        steps = [((c - r - 1) % W) for (_, r) in lst]
+        assert steps == list(range(W))               # arrival order = step order
+        g0 = (nt // group) * group
+        per_step = nM * min(group, nN - g0)          # global entries per step of this group
+        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
+        assert min(gaps) >= per_step * (W - 1) // W - W  # ranks interleave: -1 per rank
 
 
 def test_rank_column_offset_when_one_chunk_holds_all_tiles():
