@@ -98,27 +98,42 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+# The device code of the fused kernels: a recorded ncu traffic figure is valid
+# only for the source it was taken on (host-side heuristics enter through the
+# plan, which is recorded beside it).
+KERNEL_SOURCES = ("gemm_rs_kernel.cuh", "ptx.cuh", "schedule.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_gemm_reduce_tcgen05_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def plan_key(plan) -> str:
+    return "bm={bm} bn={bn} colgroup={colgroup} rowgroup={rowgroup} reduce_mode={reduce_mode}".format(**plan)
+
+
+def kernel_name(plan) -> str:
+    """The kernel a plan launches: the CTA-pair kernel for 256-row tiles."""
+    return "gemm_rs_pair_kernel" if plan["bm"] == 256 else "gemm_rs_fused_kernel"
+
+
+def recorded_traffic(kernel: str, workload: str, plan):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    if that summary was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", f"gemm_rs_fused_kernel_{workload}.md")
+    if that summary was taken on the current kernel source and the same plan."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != kernel_source_hash():
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)\s+plan:\s*([^\n]+)",
+                  text)
+    if not m or m.group(2) != kernel_source_hash() or m.group(3).strip() != plan_key(plan):
         return None
     return int(m.group(1))
 
@@ -438,6 +453,20 @@ def run_ours(args):
 
     ks_ms = time_loop(kernel_sync, args.steps, stream)
     cks_ms = time_loop(clear_kernel_sync, args.steps, stream)
+
+    # the other reduction of the library: last-arriver (rank-order fold)
+    other_mode = {}
+    mode0 = op.plan["reduce_mode"]
+    for mode, name in ((binding.GEMM_RS_REDUCE_LAST_ARRIVER, "last_arriver"),
+                       (binding.GEMM_RS_REDUCE_CHAIN, "chain")):
+        if mode == mode0:
+            continue
+        binding.gemm_rs_set_reduce_mode(op.handle, mode)
+        for _ in range(3):
+            step()
+        other_mode[name] = {"ms_per_step": time_loop(step, args.steps, stream),
+                            "plan": op.plan}
+        binding.gemm_rs_set_reduce_mode(op.handle, mode0)
     clocks = sampler.stop()
 
     # ---- roofline of the fused kernel (the only kernel of the step)
@@ -454,7 +483,8 @@ def run_ours(args):
         achieved = bytes_per_launch / (kernel_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peaks['source']} copy"}
-    roof["traffic"] = recorded_traffic(w.name)
+    roof["kernel"] = kernel_name(op.plan)
+    roof["traffic"] = recorded_traffic(roof["kernel"], w.name, op.plan)
     roof["algorithmic_bytes"] = int(bytes_per_launch)
     roof["algorithmic_flops"] = int(flops_per_launch)
     roof["kernel_ms"] = kernel_avg_ms
@@ -491,6 +521,7 @@ def run_ours(args):
                             "note": "torch.mm [M,K]x[K,N], no reduce-scatter (context)"},
             "ablation": {"kernel_batched_ms": ms_step, "kernel_sync_ms": ks_ms,
                          "clear_kernel_sync_ms": cks_ms},
+            "other_reduce_mode": other_mode,
             "plan": plan,
         }
         print(json.dumps(line))

@@ -190,9 +190,10 @@ GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
  *     Each rank's start is offset by its rank ("flux精读" §4.1), so at every
  *     step the W ranks target W different chunks.
  *   - A row tile belongs to the chunk of its first row.
- *   - The column tiles, counted from offset ((W-r) mod W)*nN/W, are split into groups of
- *     `colgroup` tiles (0 or >= nN: one group).  For each group, the rank runs
- *     all W steps.  In a step, the chunk's row tiles (ascending) are split into
+ *   - The column tiles are split into groups of `colgroup` consecutive tiles
+ *     (0 or >= nN: one group).  For each group, the rank runs all W steps.
+ *     Inside a group of gn tiles the rank starts at the group's tile
+ *     ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the chunk's row tiles (ascending) are split into
  *     row groups of `rowgroup` tiles (0: the whole chunk).  Each row group is one
  *     forward sweep over the column group's tiles.  For each column tile a
  *     sweep takes the row group's tiles in ascending order.
@@ -225,17 +226,23 @@ GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
  * tile.  Each CTA loads its own 128 rows of A and 128 columns of B, and one
  * tcgen05.mma.cta_group::2 computes the pair's product.  The default is the pair
  * kernel when there are at least four 256x256 rank-tiles per SM pair, otherwise
- * the widest single-CTA tile with at least four work items per SM. */
+ * the widest single-CTA tile with at least four work items per SM (one work item
+ * per SM when M fits in one 128-row tile). */
 GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
 
 /* Schedule shape (see gemm_rs_schedule).
- *   colgroup  column tiles per column group.  0 (the default) = one group of
- *             all column tiles.  A smaller group shortens the time between a
- *             tile's first and last rank contribution, at the cost of reading
- *             the A rows once per group.
+ *   colgroup  column tiles per column group.  0 (the default) = the
+ *             library's choice: 1, 2, 4 or 8 groups, whichever a model of the
+ *             operand bytes read from DRAM favours (A rows are read once per
+ *             group; a group's B panels of all W ranks are read once when they
+ *             fit in about 64 MB, else once per step), keeping groups large
+ *             enough that a tile's contributions arrive in step order.  A
+ *             smaller group also shortens the time between a tile's first and
+ *             last rank contribution.
  *   rowgroup  row tiles per column sweep.  0 (the default) = the library's
- *             choice: as many as keep about 48 MB of A rows (all ranks) live,
- *             capped at the chunk.  Smaller groups re-read B once per sweep.
+ *             choice: the chunk's row tiles in the fewest groups of near-equal
+ *             size that each keep at most 64 MB of A rows (all ranks) live.
+ *             Smaller groups re-read B once per sweep.
  * Returns ERR_ARG for negative values. */
 GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup);
 

@@ -209,8 +209,12 @@ int stages_for(int bm, int bn)
 int pick_bn(int64_t M, int64_t N, int W, int sms)
 {
     const int64_t nM = cdiv(M, gemm_rs::kBM);
+    // With a single row tile the call streams B once and re-reads the small A
+    // for every tile: wide tiles cut the A share of each stage, and one wave
+    // of work items is enough.
+    const int64_t waves = nM == 1 ? 1 : 4;
     for (int bn : {256, 128}) {
-        if (static_cast<int64_t>(W) * nM * cdiv(N, bn) >= 4LL * sms)
+        if (static_cast<int64_t>(W) * nM * cdiv(N, bn) >= waves * sms)
             return bn;
     }
     return 64;
@@ -218,7 +222,8 @@ int pick_bn(int64_t M, int64_t N, int W, int sms)
 
 // Launch plan: the CTA-pair kernel (256 x 256 tiles) when there are at least
 // four pair tiles per SM pair, otherwise the single-CTA kernel with the widest
-// tile that still gives at least four work items per SM.
+// tile that still gives at least four work items per SM (one when M is a
+// single row tile).
 void pick_tile(int64_t M, int64_t N, int W, int sms, int *bm, int *bn)
 {
     const int64_t pairs = static_cast<int64_t>(W) * cdiv(M, 2 * gemm_rs::kBM) * cdiv(N, 256);
@@ -232,19 +237,62 @@ void pick_tile(int64_t M, int64_t N, int W, int sms, int *bm, int *bn)
 }
 
 // Row tiles per column sweep.  A sweep keeps its row tiles' A rows live in
-// L2 for every rank at once, so bound them to about 48 MB across the W ranks.
+// L2 for every rank at once, so bound them to about 64 MB across the W ranks.
 // Returns the chunk's row tile count (one sweep per step) when that fits.
 int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm)
 {
-    const int64_t rows_per_chunk = cdiv(M / W, bm) + 1;
+    // row tiles keyed to one chunk: at most ceil(R/bm), plus one when R is ragged
+    const int64_t R = M / W;
+    const int64_t rows_per_chunk = cdiv(R, bm) + (R % bm != 0 ? 1 : 0);
     const int64_t panel = static_cast<int64_t>(bm) * Kpr * 2 * W;
-    if (panel <= 0)
-        return static_cast<int>(rows_per_chunk);
-    const int64_t budget = int64_t(48) << 20;
+    if (panel <= 0 || rows_per_chunk <= 1)
+        return static_cast<int>(rows_per_chunk > 0 ? rows_per_chunk : 1);
+    // The A rows live across the W ranks' sweeps stay within about half of L2.
+    const int64_t budget = int64_t(64) << 20;
     int64_t rg = budget / panel;
     if (rg < 1)
         rg = 1;
-    return static_cast<int>(rg < rows_per_chunk ? rg : rows_per_chunk);
+    if (rg >= rows_per_chunk)
+        return static_cast<int>(rows_per_chunk);
+    // Balanced groups: as many as the budget needs, of near-equal size.
+    const int64_t groups = cdiv(rows_per_chunk, rg);
+    return static_cast<int>(cdiv(rows_per_chunk, groups));
+}
+
+// Column tiles per group when the caller leaves it to the library.  The model
+// counts the operand bytes read from DRAM.  With k column groups, the A rows
+// of every chunk are read once per group (k * |A|).  The B panels of one group
+// are read once if the W ranks' panels of a group fit in about 64 MB of L2,
+// and once per step (W * |B|) otherwise.  k = 1, 2, 4, 8 are tried and the
+// least traffic wins (a tie keeps fewer groups).  A group must also hold
+// enough tiles that consecutive contributions to one output tile lie at least
+// 1.25 waves of workers apart, so that they arrive in step order.
+int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int64_t workers)
+{
+    const int64_t nN = cdiv(N, bn);
+    const int64_t nMs = cdiv(M, bm);
+    const double a_bytes = 2.0 * W * M * Kpr;
+    const double b_bytes = 2.0 * W * Kpr * N;
+    const double budget = 64.0 * (1 << 20);
+    int64_t best = nN;
+    double best_cost = 0.0;
+    int64_t prev = -1;
+    for (int k = 1; k <= 8; k *= 2) {
+        const int64_t G = cdiv(nN, k);
+        if (G == prev)
+            break;
+        prev = G;
+        const double sep = static_cast<double>(nMs) * G * (W - 1) / W; // work items apart
+        if (k > 1 && sep < 1.25 * static_cast<double>(workers))
+            break;
+        const double b_live = 2.0 * W * Kpr * G * bn;
+        const double cost = a_bytes * static_cast<double>(cdiv(nN, G)) + b_bytes * (b_live <= budget ? 1 : W);
+        if (k == 1 || cost < best_cost) {
+            best = G;
+            best_cost = cost;
+        }
+    }
+    return static_cast<int>(best);
 }
 
 } // namespace
@@ -257,7 +305,7 @@ struct gemm_rs_s {
     uint8_t *ws;
     Layout L;
     int device, sms, pair_clusters, bm, bn;
-    int colgroup; // 0: one group of all column tiles
+    int colgroup; // 0: the default (pick_colgroup)
     int rowgroup; // 0: the default (pick_rowgroup)
     int reduce_mode; // GEMM_RS_REDUCE_CHAIN (default) or GEMM_RS_REDUCE_LAST_ARRIVER
     CUtensorMap tmA, tmB;
@@ -266,6 +314,26 @@ struct gemm_rs_s {
     int32_t *record;
     int debug_flags;
 };
+
+namespace {
+
+// Workers of the launch: CTA pairs for the 256-row tile, CTAs otherwise.
+int64_t workers_of(const gemm_rs_s *h)
+{
+    const int64_t total = static_cast<int64_t>(h->W) * cdiv(h->M, h->bm) * cdiv(h->N, h->bn);
+    const int64_t cap = h->bm == 2 * gemm_rs::kBM ? h->pair_clusters : h->sms;
+    return total < cap ? total : cap;
+}
+
+int colgroup_of(const gemm_rs_s *h)
+{
+    const int64_t nN = cdiv(h->N, h->bn);
+    if (h->colgroup > 0)
+        return static_cast<int>(h->colgroup < nN ? h->colgroup : nN);
+    return pick_colgroup(h->M, h->N, h->Kpr, h->W, h->bm, h->bn, workers_of(h));
+}
+
+} // namespace
 
 extern "C" {
 
@@ -358,10 +426,8 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int 
         *bn = h->bn;
     if (stages)
         *stages = stages_for(h->bm, h->bn);
-    if (colgroup) {
-        const int nN = static_cast<int>(cdiv(h->N, h->bn));
-        *colgroup = (h->colgroup <= 0 || h->colgroup > nN) ? nN : h->colgroup;
-    }
+    if (colgroup)
+        *colgroup = colgroup_of(h);
     if (rowgroup)
         *rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
     if (reduce_mode)
@@ -498,7 +564,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nN = static_cast<int>(cdiv(h->N, h->bn));
     a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
-    a.colgroup = (h->colgroup <= 0 || h->colgroup > a.nN) ? a.nN : h->colgroup;
+    a.colgroup = colgroup_of(h);
     a.rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
     a.chain = h->reduce_mode == GEMM_RS_REDUCE_CHAIN ? 1 : 0;
     a.R = h->M / h->W;

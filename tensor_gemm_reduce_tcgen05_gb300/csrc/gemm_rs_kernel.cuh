@@ -26,6 +26,10 @@
 //   warps 6-9   reducers.  For each queued tile they fold the W partials in
 //               rank order in fp32, convert, and write Y.  They run beside
 //               the epilogue, so a reduction never holds a TMEM accumulator.
+//               In the chain mode (see run_epilogue) there are no queued
+//               tiles, and warps 6-9 are a second epilogue group instead:
+//               each of the eight warps drains half of its lane quarter's
+//               column slabs.
 //
 // There are no waits between CTAs.  The last arriver never waits for
 // anyone, so the kernel cannot deadlock however many CTAs it has (the
@@ -59,7 +63,7 @@ constexpr int kRedWarp0 = 6;
 constexpr int kRQ = 32;          // depth of the reduce queue (entries are quarter-tiles)
 constexpr int kConsumers = 8;    // warps that take reduce jobs: 4 reducers + 4 epilogue warps
 static_assert(kRQ >= 2 * kConsumers, "queue slots must outnumber consumers (parity reuse)");
-constexpr uint32_t kBarEpi = 1;  // named barrier of the 128 epilogue threads
+constexpr uint32_t kBarEpi = 1;  // named barrier of the epilogue threads
 constexpr int kMaxStages = 8;
 
 // Status word codes (first failure wins).
@@ -158,6 +162,10 @@ __device__ __forceinline__ void report(const KernelArgs &a, SmemCtl *ctl, uint32
         atomicCAS(a.status, 0u, code);
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
+
+// Epilogue threads: warps 2-5, or warps 2-9 in the chain mode (which has no
+// reduce jobs for warps 6-9 to take).
+__device__ __forceinline__ int epi_threads(const KernelArgs &a) { return a.chain ? 256 : 128; }
 
 // ------------------------------------------------------------------ producer
 template <int BN>
@@ -336,13 +344,13 @@ __device__ __forceinline__ bool rq_push(const KernelArgs &a, SmemCtl *ctl, uint3
 }
 
 // y = slot[lo] + slot[lo+1] + ... + slot[hi], folded left to right in fp32,
-// for one quarter (32 rows x BN columns) of tile `tile`, by one warp (lane =
-// row).  to_y: convert and write Y.  Otherwise the sum is written back to
+// for the 32-column slabs slab0 .. slab1-1 of one quarter (32 rows) of tile
+// `tile`, by one warp (lane = row).  to_y: convert and write Y.  Otherwise the sum is written back to
 // slot[hi] (a running sum).  The slots read (except a rewritten slot[hi]) are
 // dead afterwards, so their L2 lines are dropped without write-back.
 template <int BN>
 __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int q, int lane, int lo,
-                                             int hi, bool to_y)
+                                             int hi, bool to_y, int slab0, int slab1)
 {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::kSlabs;
@@ -353,49 +361,39 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
     // slot 0's 32-row quarter; slot s's is s * kSlotFloats further on
     float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                 static_cast<int64_t>(q) * S * 1024;
-    const int n_in = hi - lo + 1;
 #pragma unroll 1
-    for (int slab = 0; slab < S; ++slab) {
-        const float *sb = qb + static_cast<int64_t>(lo) * Cfg::kSlotFloats + slab * 1024 + lane * 4;
-        float4 prev_half = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int slab = slab0; slab < slab1; ++slab) {
+        // One slab of a slot is 8 float4 per lane (a 4 KB block per warp),
+        // loaded at once.  Fixed order: y = slot[lo], then y = y + slot[s].
+        const float *sb = qb + slab * 1024 + lane * 4;
+        float4 y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(lo) * Cfg::kSlotFloats + j * 128);
 #pragma unroll 1
-        for (int jf = 0; jf < 8; ++jf) {
-            // float4 j = jf: columns 4*jf .. 4*jf+3 of the slab.
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < n_in; s0 += 8) {
-                float4 u[8];
+        for (int sl = lo + 1; sl <= hi; ++sl) {
+            float4 u[8];
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu)
-                    if (s0 + uu < n_in)
-                        u[uu] = ptx::ld_cg_f4(sb + static_cast<int64_t>(s0 + uu) * Cfg::kSlotFloats +
-                                              jf * 128);
-                // Fixed order: y = slot[lo], then y = y + slot[s].
+            for (int j = 0; j < 8; ++j)
+                u[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(sl) * Cfg::kSlotFloats + j * 128);
 #pragma unroll
-                for (int uu = 0; uu < 8; ++uu) {
-                    if (s0 + uu < n_in) {
-                        if (s0 + uu == 0) {
-                            y = u[uu];
-                        } else {
-                            y.x += u[uu].x; y.y += u[uu].y; y.z += u[uu].z; y.w += u[uu].w;
-                        }
-                    }
-                }
+            for (int j = 0; j < 8; ++j) {
+                y[j].x += u[j].x; y[j].y += u[j].y; y[j].z += u[j].z; y[j].w += u[j].w;
             }
-            if (to_y) {
-                // Y is written 8 columns at a time: keep the even float4 until
-                // its odd neighbour is done.
-                if ((jf & 1) == 0) {
-                    prev_half = y;
-                } else {
-                    const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + (jf - 1) * 4;
-                    if (row_ok && n < a.N) // N is a multiple of 8
-                        store_y8(a, m, n, prev_half, y);
-                }
-            } else {
-                ptx::st_f4(qb + static_cast<int64_t>(hi) * Cfg::kSlotFloats + slab * 1024 + lane * 4 +
-                               jf * 128,
-                           y);
+        }
+        if (to_y) {
+            // Y is written 8 columns at a time.
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) {
+                const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + j2 * 8;
+                if (row_ok && n < a.N) // N is a multiple of 8
+                    store_y8(a, m, n, y[2 * j2], y[2 * j2 + 1]);
             }
+        } else {
+            float *dst = qb + static_cast<int64_t>(hi) * Cfg::kSlotFloats + slab * 1024 + lane * 4;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                ptx::st_f4(dst + j * 128, y[j]);
         }
         // Every lane has read this slab of every slot: drop the dead lines
         // (lane l drops line l of each 4 KB block).
@@ -418,10 +416,15 @@ constexpr uint32_t kChainOwn = 1u << 24;
 __device__ __forceinline__ uint32_t chain_k(uint32_t s) { return (s >> 16) & 31u; }
 
 // Take the fold at position i: true if positions 0 .. i-1 are folded, nobody
-// owns the tile, and the caller now owns it.
+// owns the tile, and the caller now owns it.  The first compare-and-swap
+// guesses the usual state (k = i, nothing stored ahead), so the common case
+// costs one atomic.
 __device__ __forceinline__ bool chain_try_own(uint32_t *flag, uint32_t i)
 {
-    uint32_t s = ptx::ld_acquire_gpu(flag);
+    const uint32_t guess = i << 16;
+    uint32_t s = ptx::atom_cas_acq_rel_gpu(flag, guess, guess | kChainOwn);
+    if (s == guess)
+        return true;
     while (chain_k(s) == i && !(s & kChainOwn)) {
         const uint32_t prev = ptx::atom_cas_acq_rel_gpu(flag, s, s | kChainOwn);
         if (prev == s)
@@ -434,9 +437,13 @@ __device__ __forceinline__ bool chain_try_own(uint32_t *flag, uint32_t i)
 // The owner has folded positions 0 .. kn-1 (running sum in slot kn-1).  If
 // position kn is already stored, it keeps the ownership and returns true (the
 // caller folds on from kn).  Otherwise it publishes k = kn and releases.
-__device__ __forceinline__ bool chain_pass_on(uint32_t *flag, uint32_t kn)
+// `guess` is the state the caller expects; a wrong guess costs one more
+// compare-and-swap.  The release side of the compare-and-swap publishes the
+// running sum, which every epilogue thread stored before the CTA barrier that
+// precedes this call.
+__device__ __forceinline__ bool chain_pass_on(uint32_t *flag, uint32_t kn, uint32_t guess)
 {
-    uint32_t s = ptx::ld_acquire_gpu(flag);
+    uint32_t s = guess;
     while (true) {
         if ((s >> kn) & 1u)
             return true;
@@ -477,7 +484,7 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
         }
         if (entry < 0)
             break;
-        fold_quarter<BN>(a, entry >> 2, entry & 3, lane, 0, a.W - 1, true);
+        fold_quarter<BN>(a, entry >> 2, entry & 3, lane, 0, a.W - 1, true, 0, TileCfg<BN>::kSlabs);
     }
 }
 
@@ -494,7 +501,9 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
 // writing slot i, or Y at the last position.  A rank that is early stores its
 // partial in slot i.  Whoever owns the fold when the positions after it are
 // already stored (or the early rank itself, once its turn has come) folds
-// them from their slots with all four epilogue warps, one quarter each.
+// them from their slots.  The chain mode has no reduce jobs, so warps 6-9 join
+// the epilogue: two warps per TMEM lane quarter, each draining half of the
+// tile's 32-column slabs.
 template <int BN, bool PAIR>
 __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &sch, uint32_t tmem,
                                              SmemCtl *ctl, int warp, int lane, int64_t g0,
@@ -503,7 +512,12 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     using Cfg = TileCfg<BN>;
     const volatile int *abort_flag = &ctl->abort;
     const int q = warp & 3;                           // TMEM lanes [32q, 32q + 32)
-    const int etid = threadIdx.x - kEpiWarp0 * 32;    // 0 .. 127
+    const int etid = threadIdx.x - kEpiWarp0 * 32;    // 0 .. nthr-1
+    const int nthr = epi_threads(a);
+    // slabs [sl0, sl1) of every tile: all of them with one warp per quarter
+    const int half = (warp - kEpiWarp0) >> 2;
+    const int sl0 = a.chain ? half * (Cfg::kSlabs / 2) : 0;
+    const int sl1 = a.chain ? sl0 + Cfg::kSlabs / 2 : Cfg::kSlabs;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     // Last-arriver partials are read back only at the end of the schedule: do
     // not let them push the B panels out of L2.  Chain-mode slots are read at
@@ -528,7 +542,11 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
                                  : ptx::mbar_wait(fb, aph, a.timeout, abort_flag);
-        if (ptx::named_bar_or(kBarEpi, 128, !(waited && ok))) {
+        // If position step-1 was not folded yet at the start, it may be by the
+        // time the accumulator lands: try once more before storing.
+        if (etid == 0 && a.chain && waited && half_ok && ctl->epi_direct[buf] == 0)
+            ctl->epi_direct[buf] = chain_try_own(a.flags + tile, static_cast<uint32_t>(step)) ? 1 : 0;
+        if (ptx::named_bar_or(kBarEpi, nthr, !(waited && ok))) {
             ok = false;
             break;
         }
@@ -555,21 +573,15 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
         float *slot = tb + static_cast<int64_t>(sidx) * Cfg::kSlotFloats;
         const float *prev = tb + static_cast<int64_t>(step > 0 ? step - 1 : 0) * Cfg::kSlotFloats;
-        // The running sum of slot step-1 is loaded one slab ahead, so its
-        // latency overlaps the previous slab's work.
-        float4 rs[8];
-        if (add_prev) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                rs[j] = ptx::ld_cg_f4(prev + j * 128);
-        }
+        // The running sum of slot step-1 is loaded before the slab's TMEM
+        // read; the other warp of the lane quarter covers its latency.
 #pragma unroll 1
-        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
-            float4 rn[8];
-            if (add_prev && slab + 1 < Cfg::kSlabs) {
+        for (int slab = sl0; slab < sl1; ++slab) {
+            float4 rs[8];
+            if (add_prev) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    rn[j] = ptx::ld_cg_f4(prev + (slab + 1) * 1024 + j * 128);
+                    rs[j] = ptx::ld_cg_f4(prev + slab * 1024 + j * 128);
             }
             uint32_t v[32];
             if (a.nK > 0) {
@@ -580,8 +592,9 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 for (int i = 0; i < 32; ++i)
                     v[i] = 0u;
             }
-            if (slab == Cfg::kSlabs - 1) {
-                // The accumulator is fully read: hand it back to the MMA thread.
+            if (slab == sl1 - 1) {
+                // The warp's share of the accumulator is read: hand it back to
+                // the MMA thread.
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -644,17 +657,15 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 // slot step-1 is dead: drop its lines of this warp's 4 KB block
                 __syncwarp();
                 ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    rs[j] = rn[j];
             }
         }
 
-        // Every epilogue thread has issued its stores.  Publish them at gpu
-        // scope, then take the tile's next step.
-        ptx::named_bar_sync(kBarEpi, 128);
+        // Every epilogue thread has issued its stores.  The barrier orders them
+        // before thread 0's flag atomic, whose release side publishes them at
+        // gpu scope; the thread that acquires the flag, and through the next
+        // barrier its CTA, then sees them.
+        ptx::named_bar_sync(kBarEpi, nthr);
         if (etid == 0) {
-            __threadfence();
             uint32_t *flag = a.flags + tile;
             if (!a.chain) {
                 const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
@@ -670,7 +681,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 if (direct) {
                     if (to_y)
                         ptx::st_relaxed_gpu(flag, 0u); // back to 0 for the next call
-                    else if (chain_pass_on(flag, static_cast<uint32_t>(step + 1)))
+                    else if (chain_pass_on(flag, static_cast<uint32_t>(step + 1),
+                                           (static_cast<uint32_t>(step) << 16) | kChainOwn))
                         fold_from = step + 1;
                 } else {
                     const uint32_t old = ptx::atom_or_acq_rel_gpu(flag, 1u << step);
@@ -683,8 +695,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         }
         if (a.chain) {
             // Fold on while the positions after the running sum are already
-            // stored: every warp takes its own quarter of the tile.
-            ptx::named_bar_sync(kBarEpi, 128);
+            // stored: every warp takes its own slabs of its quarter.
+            ptx::named_bar_sync(kBarEpi, nthr);
             int k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
             while (k >= 0) {
                 uint32_t *flag = a.flags + tile;
@@ -695,33 +707,34 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                         ++j;
                     ctl->epi_fold_end = j;
                 }
-                ptx::named_bar_sync(kBarEpi, 128);
+                ptx::named_bar_sync(kBarEpi, nthr);
                 const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
-                fold_quarter<BN>(a, tile, q, lane, k > 0 ? k - 1 : k, j, j == a.W - 1);
-                ptx::named_bar_sync(kBarEpi, 128);
+                fold_quarter<BN>(a, tile, q, lane, k > 0 ? k - 1 : k, j, j == a.W - 1, sl0, sl1);
+                ptx::named_bar_sync(kBarEpi, nthr);
                 if (etid == 0) {
-                    __threadfence();
                     int next = -1;
                     if (j == a.W - 1)
                         ptx::st_relaxed_gpu(flag, 0u);
-                    else if (chain_pass_on(flag, static_cast<uint32_t>(j + 1)))
+                    else if (chain_pass_on(flag, static_cast<uint32_t>(j + 1),
+                                           ptx::ld_acquire_gpu(flag)))
                         next = j + 1;
                     ctl->epi_fold = next;
                 }
-                ptx::named_bar_sync(kBarEpi, 128);
+                ptx::named_bar_sync(kBarEpi, nthr);
                 k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
             }
         }
     }
-    // No more tiles: one stop entry per consumer warp.
+    // No more tiles: one stop entry per consumer warp (last-arriver mode).
     if (etid == 0) {
-        for (int i = 0; i < kConsumers && ok; ++i)
-            ok = rq_push(a, ctl, rq_n, -1);
+        if (!a.chain)
+            for (int i = 0; i < kConsumers && ok; ++i)
+                ok = rq_push(a, ctl, rq_n, -1);
         if (!ok)
             report(a, ctl, kStatusTimeoutEpilogue);
     }
     // Once its own tiles are done, the epilogue helps with the reductions.
-    if (!ptx::named_bar_or(kBarEpi, 128, !ok))
+    if (!ptx::named_bar_or(kBarEpi, nthr, !ok) && !a.chain)
         run_consumer<BN>(a, ctl, lane);
 }
 
@@ -746,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&ctl->acc_full[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 4);
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), epi_threads(a) / 32);
         }
         for (int s = 0; s < kRQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
@@ -779,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0)
             run_mma<BN>(a, tmem, smem, ctl);
         __syncwarp();
-    } else if (warp < kRedWarp0) {
+    } else if (warp < kRedWarp0 || a.chain) {
         run_epilogue<BN, false>(a, sch, tmem, ctl, warp, lane, blockIdx.x, gridDim.x, 0u);
     } else {
         run_consumer<BN>(a, ctl, lane);
@@ -971,7 +984,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&ctl->acc_full[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 8); // 4 epilogue warps x 2 CTAs
+            // epilogue warps x 2 CTAs
+            ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 2 * (epi_threads(a) / 32));
         }
         for (int s = 0; s < kRQ; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctl->rq_full[s]), 1);
@@ -1005,7 +1019,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0 && crank == 0)
             run_mma_pair<BN>(a, tmem, smem, ctl);
         __syncwarp();
-    } else if (warp < kRedWarp0) {
+    } else if (warp < kRedWarp0 || a.chain) {
         run_epilogue<BN, true>(a, sch, tmem, ctl, warp, lane, blockIdx.x / 2, gridDim.x / 2, crank);
     } else {
         run_consumer<BN>(a, ctl, lane);
