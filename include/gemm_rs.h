@@ -249,7 +249,9 @@ GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup);
 /* Select the reduction (GEMM_RS_REDUCE_*).  Both give Y within the stated
  * tolerances of each other.  Each is bit-identical from run to run.  They
  * differ in summation order: rank order 0..W-1 for LAST_ARRIVER, the steps'
- * order for CHAIN.  ERR_ARG for other values. */
+ * order for CHAIN.  CHAIN adds the middle positions to the running sum in L2
+ * (red.add.f32), which flushes subnormal sums to zero.  ERR_ARG for other
+ * values. */
 GEMM_RS_API int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode);
 
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);

@@ -343,11 +343,14 @@ __device__ __forceinline__ bool rq_push(const KernelArgs &a, SmemCtl *ctl, uint3
     return true;
 }
 
-// y = slot[lo] + slot[lo+1] + ... + slot[hi], folded left to right in fp32,
-// for the 32-column slabs slab0 .. slab1-1 of one quarter (32 rows) of tile
-// `tile`, by one warp (lane = row).  to_y: convert and write Y.  Otherwise the sum is written back to
-// slot[hi] (a running sum).  The slots read (except a rewritten slot[hi]) are
-// dead afterwards, so their L2 lines are dropped without write-back.
+// y = slot[0] + slot[f] + slot[f+1] + ... + slot[hi] with f = max(lo, 1),
+// folded left to right in fp32, for the 32-column slabs slab0 .. slab1-1 of
+// one quarter (32 rows) of tile `tile`, by one warp (lane = row).  Slot 0
+// holds the running sum (chain mode) or rank 0's partial (last-arriver mode,
+// lo = 0: the W partials in rank order).  to_y: convert and write Y.
+// Otherwise the sum is written back to slot 0.  The slots f .. hi (and slot 0
+// after writing Y) are dead afterwards, so their L2 lines are dropped without
+// write-back.
 template <int BN>
 __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int q, int lane, int lo,
                                              int hi, bool to_y, int slab0, int slab1)
@@ -361,17 +364,18 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
     // slot 0's 32-row quarter; slot s's is s * kSlotFloats further on
     float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                 static_cast<int64_t>(q) * S * 1024;
+    const int first = lo > 1 ? lo : 1;
 #pragma unroll 1
     for (int slab = slab0; slab < slab1; ++slab) {
         // One slab of a slot is 8 float4 per lane (a 4 KB block per warp),
-        // loaded at once.  Fixed order: y = slot[lo], then y = y + slot[s].
+        // loaded at once.  Fixed order: y = slot[0], then y = y + slot[s].
         const float *sb = qb + slab * 1024 + lane * 4;
         float4 y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            y[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(lo) * Cfg::kSlotFloats + j * 128);
+            y[j] = ptx::ld_cg_f4(sb + j * 128);
 #pragma unroll 1
-        for (int sl = lo + 1; sl <= hi; ++sl) {
+        for (int sl = first; sl <= hi; ++sl) {
             float4 u[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -390,7 +394,7 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
                     store_y8(a, m, n, y[2 * j2], y[2 * j2 + 1]);
             }
         } else {
-            float *dst = qb + static_cast<int64_t>(hi) * Cfg::kSlotFloats + slab * 1024 + lane * 4;
+            float *dst = qb + slab * 1024 + lane * 4;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 ptx::st_f4(dst + j * 128, y[j]);
@@ -398,8 +402,9 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
         // Every lane has read this slab of every slot: drop the dead lines
         // (lane l drops line l of each 4 KB block).
         __syncwarp();
-        const int last_dead = to_y ? hi : hi - 1;
-        for (int s = lo; s <= last_dead; ++s)
+        if (to_y)
+            ptx::discard_l2_line(qb + slab * 1024 + lane * 32);
+        for (int s = first; s <= hi; ++s)
             ptx::discard_l2_line(qb + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 +
                                  lane * 32);
     }
@@ -408,11 +413,15 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
 // ---------------------------------------------------------------- chain reduction state
 // In the chain mode each output tile has one 32-bit state word:
 //   bits  0-15  positions whose partial is stored in their slot and not yet folded
-//   bits 16-20  k: positions 0 .. k-1 are folded; their running sum is in slot k-1
+//   bits 16-20  k: positions 0 .. k-1 are folded; their running sum is in slot 0
 //   bit  24     owned: one CTA is folding from position k on
 // Position i is the step in which its rank reaches the tile, so in a steady run
 // the positions arrive in order and each one folds itself straight from TMEM.
+// The flag's release/acquire chain orders the folds: position i's additions
+// to slot 0 all happen before position i+1's, so every element is summed in
+// position order, the same order on every run.
 constexpr uint32_t kChainOwn = 1u << 24;
+constexpr long long kChainWaitCycles = 16384; // how long a position waits for its turn
 __device__ __forceinline__ uint32_t chain_k(uint32_t s) { return (s >> 16) & 31u; }
 
 // Take the fold at position i: true if positions 0 .. i-1 are folded, nobody
@@ -434,7 +443,7 @@ __device__ __forceinline__ bool chain_try_own(uint32_t *flag, uint32_t i)
     return false;
 }
 
-// The owner has folded positions 0 .. kn-1 (running sum in slot kn-1).  If
+// The owner has folded positions 0 .. kn-1 (running sum in slot 0).  If
 // position kn is already stored, it keeps the ownership and returns true (the
 // caller folds on from kn).  Otherwise it publishes k = kn and releases.
 // `guess` is the state the caller expects; a wrong guess costs one more
@@ -452,6 +461,24 @@ __device__ __forceinline__ bool chain_pass_on(uint32_t *flag, uint32_t kn, uint3
         if (prev == s)
             return false;
         s = prev;
+    }
+}
+
+// Wait for the turn of position i (positions 0 .. i-1 folded), then take the
+// fold.  The wait is bounded by `limit` SM cycles: after that the caller stores
+// its partial and the fold happens later.  Waiting cannot deadlock: position
+// i-1 lies earlier in the global tile order, and a CTA that waits only ever
+// waits for earlier items; the bound keeps even a stalled peer from holding it.
+__device__ __forceinline__ bool chain_wait_own(uint32_t *flag, uint32_t i, long long limit)
+{
+    const long long t0 = clock64();
+    while (true) {
+        const uint32_t s = ptx::ld_acquire_gpu(flag);
+        if (chain_k(s) == i && !(s & kChainOwn) && chain_try_own(flag, i))
+            return true;
+        if (chain_k(s) > i || clock64() - t0 > limit)
+            return false;
+        __nanosleep(64);
     }
 }
 
@@ -497,9 +524,10 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
 // on the tile's counter, and the rank that arrives last queues the tile: the
 // consumers fold slots 0 .. W-1 (rank order) into Y.
 // Chain mode: the rank at position i (its step) folds its own partial straight
-// from TMEM onto the running sum in slot i-1 when positions 0 .. i-1 are done,
-// writing slot i, or Y at the last position.  A rank that is early stores its
-// partial in slot i.  Whoever owns the fold when the positions after it are
+// from TMEM onto the running sum in slot 0 when positions 0 .. i-1 are done:
+// position 0 stores it, positions 1 .. W-2 add to it in L2 (red.add, nothing
+// comes back to the SM), and the last position reads it and writes Y.  A rank
+// that is early stores its partial in slot i.  Whoever owns the fold when the positions after it are
 // already stored (or the early rank itself, once its turn has come) folds
 // them from their slots.  The chain mode has no reduce jobs, so warps 6-9 join
 // the epilogue: two warps per TMEM lane quarter, each draining half of the
@@ -542,10 +570,13 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
                                  : ptx::mbar_wait(fb, aph, a.timeout, abort_flag);
-        // If position step-1 was not folded yet at the start, it may be by the
-        // time the accumulator lands: try once more before storing.
+        // If position step-1 was not folded yet at the start, wait a little for
+        // it now that the accumulator has landed: a store and a later fold
+        // cost far more.  Late positions come mostly from the first step of a
+        // column group, whose B panels are not in L2 yet.
         if (etid == 0 && a.chain && waited && half_ok && ctl->epi_direct[buf] == 0)
-            ctl->epi_direct[buf] = chain_try_own(a.flags + tile, static_cast<uint32_t>(step)) ? 1 : 0;
+            ctl->epi_direct[buf] =
+                chain_wait_own(a.flags + tile, static_cast<uint32_t>(step), kChainWaitCycles) ? 1 : 0;
         if (ptx::named_bar_or(kBarEpi, nthr, !(waited && ok))) {
             ok = false;
             break;
@@ -563,18 +594,22 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             continue;
         }
         const bool direct = *reinterpret_cast<volatile int *>(&ctl->epi_direct[buf]) != 0;
-        const int sidx = a.chain ? step : r;                 // slot written
+        // Chain mode: the running sum lives in slot 0.  Position 0 stores it,
+        // positions 1 .. W-2 add to it in L2, and the last position reads it
+        // and writes Y.  An early position stores its partial in its own slot.
+        const int sidx = a.chain ? (direct ? 0 : step) : r;  // slot written
         const bool to_y = direct && step == a.W - 1;         // the last fold writes Y
-        const bool add_prev = direct && step > 0;            // fold onto slot step-1
+        const bool add_prev = to_y && step > 0;              // read the running sum
+        const bool add_l2 = direct && step > 0 && !to_y;     // add to it in L2
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
         float *tb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                     static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
         float *slot = tb + static_cast<int64_t>(sidx) * Cfg::kSlotFloats;
-        const float *prev = tb + static_cast<int64_t>(step > 0 ? step - 1 : 0) * Cfg::kSlotFloats;
-        // The running sum of slot step-1 is loaded before the slab's TMEM
-        // read; the other warp of the lane quarter covers its latency.
+        const float *prev = tb; // slot 0: the running sum
+        // The running sum is loaded before the slab's TMEM read; the other
+        // warp of the lane quarter covers its latency.
 #pragma unroll 1
         for (int slab = sl0; slab < sl1; ++slab) {
             float4 rs[8];
@@ -645,6 +680,13 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                                  make_float4(p[8 * g8], p[8 * g8 + 1], p[8 * g8 + 2], p[8 * g8 + 3]),
                                  make_float4(p[8 * g8 + 4], p[8 * g8 + 5], p[8 * g8 + 6], p[8 * g8 + 7]));
                 }
+            } else if (add_l2) {
+                // running sum + this position's partial, added in L2
+                float *dst = slot + slab * 1024;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ptx::red_add_f4(dst + j * 128,
+                                    make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
             } else {
                 float *dst = slot + slab * 1024;
 #pragma unroll
@@ -654,7 +696,7 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                                     st_pol);
             }
             if (add_prev) {
-                // slot step-1 is dead: drop its lines of this warp's 4 KB block
+                // the running sum is dead: drop its lines of this warp's 4 KB block
                 __syncwarp();
                 ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
             }
@@ -709,7 +751,7 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 }
                 ptx::named_bar_sync(kBarEpi, nthr);
                 const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
-                fold_quarter<BN>(a, tile, q, lane, k > 0 ? k - 1 : k, j, j == a.W - 1, sl0, sl1);
+                fold_quarter<BN>(a, tile, q, lane, k, j, j == a.W - 1, sl0, sl1);
                 ptx::named_bar_sync(kBarEpi, nthr);
                 if (etid == 0) {
                     int next = -1;

@@ -433,6 +433,16 @@ __device__ __forceinline__ void st_f4_hint(float *p, float4 v, uint64_t policy)
                  : "memory");
 }
 
+// Four fp32 additions performed in L2 (relaxed, gpu scope): *p += v, element
+// by element, rounded to nearest even.  The L2 flushes subnormal inputs and
+// results to zero.  Nothing comes back to the SM.
+__device__ __forceinline__ void red_add_f4(float *p, float4 v)
+{
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 // Drop one 128-byte L2 line without writing it back.  Its contents become
 // undefined, so this is only for data that is dead: read for the last time,
 // and written again before it is next read.
