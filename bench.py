@@ -115,7 +115,8 @@ def kernel_source_hash() -> str:
 
 
 def plan_key(plan) -> str:
-    return "bm={bm} bn={bn} colgroup={colgroup} rowgroup={rowgroup} reduce_mode={reduce_mode}".format(**plan)
+    return ("bm={bm} bn={bn} colgroup={colgroup} rowgroup={rowgroup} rank_order={rank_order} "
+            "reduce_mode={reduce_mode}").format(**plan)
 
 
 def kernel_name(plan) -> str:

@@ -85,15 +85,25 @@ enum {
 
 /* How the W partials of an output tile are reduced (gemm_rs_set_reduce_mode). */
 enum {
-    /* Default.  The ranks fold into the tile in the order of the steps at which
-     * they reach it (a fixed order per tile).  The rank whose turn it is adds
-     * its accumulator straight from TMEM onto the running sum.  A rank that is
-     * early stores its partial, and the current owner of the fold picks it up.
-     * The rank at the last step writes Y.  The reduction overlaps the GEMM. */
+    /* Default.  The ranks fold into the tile in the order in which the
+     * schedule brings them to it (a fixed order per tile: rank order 0..W-1
+     * when the ranks run one after another, the order of their steps when they
+     * run side by side).  The rank whose turn it is adds its accumulator
+     * straight from TMEM onto the running sum.  A rank that is early stores its
+     * partial, and the current owner of the fold picks it up.  The last rank
+     * writes Y.  The reduction overlaps the GEMM. */
     GEMM_RS_REDUCE_CHAIN = 0,
     /* Every rank stores its partial.  The last rank to arrive at a tile folds
      * all W partials in rank order 0 .. W-1 and writes Y. */
     GEMM_RS_REDUCE_LAST_ARRIVER = 1
+};
+
+/* The order in which the W logical ranks' tiles run (gemm_rs_set_schedule). */
+enum {
+    GEMM_RS_RANKS_DEFAULT = 0,     /* the library's choice: SEQUENTIAL */
+    GEMM_RS_RANKS_SEQUENTIAL = 1,  /* rank 0's tiles, then rank 1's, ...: one rank's
+                                      operands are live at a time */
+    GEMM_RS_RANKS_INTERLEAVED = 2  /* the W ranks side by side, as W GPUs would run */
 };
 
 /* Debug flags for gemm_rs_set_debug. */
@@ -187,40 +197,44 @@ GEMM_RS_API int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream);
  *   - Rank r visits its chunks in the order (r+1+s) mod W, s = 0 .. W-1:
  *     the remote chunks first and its own chunk r last
  *     ("flux实现：sm80 gemm+rs", section "gemmrs版本的swizzle如何编排").
- *     Each rank's start is offset by its rank ("flux精读" §4.1), so at every
- *     step the W ranks target W different chunks.
+ *     Each rank's start is offset by its rank ("flux精读" §4.1), so when the
+ *     ranks run side by side the W ranks target W different chunks at every
+ *     step.
  *   - A row tile belongs to the chunk of its first row.
  *   - The column tiles are split into groups of `colgroup` consecutive tiles
  *     (0 or >= nN: one group).  For each group, the rank runs all W steps.
  *     Inside a group of gn tiles the rank starts at the group's tile
- *     ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the chunk's row tiles (ascending) are split into
- *     row groups of `rowgroup` tiles (0: the whole chunk).  Each row group is one
- *     forward sweep over the column group's tiles.  For each column tile a
- *     sweep takes the row group's tiles in ascending order.
- *   - Entry p*W + r is rank r's p-th tile: the ranks advance side by side.
+ *     ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the
+ *     chunk's row tiles (ascending) are split into row groups of `rowgroup`
+ *     tiles (0: the whole chunk).  Each row group is one forward sweep over
+ *     the column group's tiles.  For each column tile a sweep takes the row
+ *     group's tiles in ascending order.
+ *   - rank_order GEMM_RS_RANKS_INTERLEAVED: entry p*W + r is rank r's p-th
+ *     tile (the ranks advance side by side).  GEMM_RS_RANKS_SEQUENTIAL or
+ *     GEMM_RS_RANKS_DEFAULT: entry r*T + p is rank r's p-th tile, T = nM*nN
+ *     (one rank after another).
  * `cap` is the capacity of `out` in triples.  Returns the number of entries,
  * or a negative error code (ERR_SHAPE if cap is too small).
  */
 GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup,
-                                     int rowgroup, int32_t *out, int64_t cap);
+                                     int rowgroup, int rank_order, int32_t *out, int64_t cap);
 
 /*
  * Launch plan of the handle (host outputs; any pointer may be NULL):
  *   bm, bn   the output tile (bm = 128; bn = 256, 128 or 64)
  *   stages   depth of the TMA -> MMA shared-memory ring
  *   grid     CTAs launched (persistent: one per SM, at most one per work item)
- *   colgroup, rowgroup  the schedule shape in effect (see gemm_rs_set_schedule)
+ *   colgroup, rowgroup, rank_order  the schedule in effect (see gemm_rs_set_schedule;
+ *                       rank_order is GEMM_RS_RANKS_SEQUENTIAL or _INTERLEAVED)
  *   reduce_mode         GEMM_RS_REDUCE_CHAIN or GEMM_RS_REDUCE_LAST_ARRIVER
  */
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
-                                 int *colgroup, int *rowgroup, int *reduce_mode);
+                                 int *colgroup, int *rowgroup, int *rank_order, int *reduce_mode);
 
 /* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
  * (bm = 128).  Returns ERR_ARG for any other value. */
 GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
 
-/* Device wait limit in SM clock cycles (default 2^32, about two seconds).  A
- * wait that runs past it sets the status word and lets the kernel exit. */
 /* Override the output tile.  (128, 64|128|256) runs the single-CTA kernel.
  * (256, 256) runs the CTA-pair kernel: a cluster of two CTAs shares one 256x256
  * tile.  Each CTA loads its own 128 rows of A and 128 columns of B, and one
@@ -230,30 +244,34 @@ GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);
  * per SM when M fits in one 128-row tile). */
 GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
 
-/* Schedule shape (see gemm_rs_schedule).
- *   colgroup  column tiles per column group.  0 (the default) = the
- *             library's choice: 1, 2, 4 or 8 groups, whichever a model of the
- *             operand bytes read from DRAM favours (A rows are read once per
- *             group; a group's B panels of all W ranks are read once when they
- *             fit in about 64 MB, else once per step), keeping groups large
- *             enough that a tile's contributions arrive in step order.  A
- *             smaller group also shortens the time between a tile's first and
- *             last rank contribution.
- *   rowgroup  row tiles per column sweep.  0 (the default) = the library's
- *             choice: the chunk's row tiles in the fewest groups of near-equal
- *             size that each keep at most 64 MB of A rows (all ranks) live.
- *             Smaller groups re-read B once per sweep.
- * Returns ERR_ARG for negative values. */
-GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup);
+/* Schedule (see gemm_rs_schedule).  "Live ranks" below is 1 for the
+ * sequential rank order and W for the interleaved one.
+ *   colgroup    column tiles per column group.  0 (the default) = the
+ *               library's choice: 1, 2, 4 or 8 groups, whichever a model of
+ *               the operand bytes read from DRAM favours (A rows are read once
+ *               per group; a group's B panels of the live ranks are read once
+ *               when they fit in about 64 MB, else once per step); with the
+ *               ranks side by side, groups stay large enough that a tile's
+ *               contributions arrive in step order.
+ *   rowgroup    row tiles per column sweep.  0 (the default) = the library's
+ *               choice: the chunk's row tiles in the fewest groups of
+ *               near-equal size that each keep at most 64 MB of A rows of the
+ *               live ranks.  Smaller groups re-read B once per sweep.
+ *   rank_order  GEMM_RS_RANKS_* (0: the default, SEQUENTIAL).
+ * Returns ERR_ARG for negative values or an unknown rank order. */
+GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup, int rank_order);
 
 /* Select the reduction (GEMM_RS_REDUCE_*).  Both give Y within the stated
  * tolerances of each other.  Each is bit-identical from run to run.  They
- * differ in summation order: rank order 0..W-1 for LAST_ARRIVER, the steps'
- * order for CHAIN.  CHAIN adds the middle positions to the running sum in L2
+ * differ in summation order: rank order 0..W-1 for LAST_ARRIVER, the
+ * schedule's arrival order for CHAIN (the same rank order with the default
+ * sequential ranks).  CHAIN adds the middle positions to the running sum in L2
  * (red.add.f32), which flushes subnormal sums to zero.  ERR_ARG for other
  * values. */
 GEMM_RS_API int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode);
 
+/* Device wait limit in SM clock cycles (default 2^32, about two seconds).  A
+ * wait that runs past it sets the status word and lets the kernel exit. */
 GEMM_RS_API int gemm_rs_set_timeout_cycles(gemm_rs_t h, uint64_t cycles);
 
 /*

@@ -51,7 +51,7 @@ def _load():
         lib.oracle_gemm_rs.argtypes = [i32, i64, i64, i64, f32, f32, vp, vp, vp,
                                        i32, vp, i64, vp, vp, i32]
         lib.oracle_schedule.restype = i64
-        lib.oracle_schedule.argtypes = [i32, i64, i64, i32, i32, i32, i32, vp, i64]
+        lib.oracle_schedule.argtypes = [i32, i64, i64, i32, i32, i32, i32, i32, vp, i64]
         lib.oracle_row_chunk.restype = i32
         lib.oracle_row_chunk.argtypes = [i32, i64, vp, vp]
         lib.oracle_bf16_from_float.restype = None
@@ -104,12 +104,18 @@ def gemm_rs(A: np.ndarray, B: np.ndarray, C: np.ndarray | None, alpha: float, be
     return out
 
 
-def schedule(W: int, M: int, N: int, BM: int, BN: int, G: int = 0, RG: int = 0) -> np.ndarray:
+def schedule(W: int, M: int, N: int, BM: int, BN: int, G: int = 0, RG: int = 0,
+             order: str = "interleaved") -> np.ndarray:
     """Global tile order as an int32 [W*nM*nN, 3] array of (r, mt, nt).
-    G = column tiles per group (0: one group); RG = row tiles per sweep (0: whole chunk)."""
+    G = column tiles per group (0: one group); RG = row tiles per sweep (0: whole chunk);
+    order = "interleaved" (the W ranks side by side) or "sequential" (one rank after
+    another)."""
+    if order not in ("interleaved", "sequential"):
+        raise ValueError(f"unknown rank order {order!r}")
     nM, nN = -(-M // BM), -(-N // BN)
     out = np.zeros((W * nM * nN, 3), dtype=np.int32)
-    n = _load().oracle_schedule(W, M, N, BM, BN, G, RG, out.ctypes.data, out.shape[0])
+    n = _load().oracle_schedule(W, M, N, BM, BN, G, RG, 1 if order == "sequential" else 0,
+                                out.ctypes.data, out.shape[0])
     if n < 0:
         raise ValueError(f"oracle_schedule rejected its arguments (rc={n})")
     return out[:n]

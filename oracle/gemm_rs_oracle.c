@@ -185,16 +185,18 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
  *  - The column tiles form groups of G consecutive tiles (G <= 0 or G >= nN: a
  *    single group).  For each group, in order, the rank runs all W steps.
  *    Inside a group of gn tiles the rank starts at the group's tile
- *    ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the chunk's row tiles (ascending) are split
- *    into row groups of RG tiles (RG <= 0: the whole chunk).  Each row group is
- *    one forward sweep over the group's column tiles.  For each column tile a
- *    sweep takes the row group's tiles in ascending order.
- *  - The W ranks run side by side: entry p*W + r of the global order is the
- *    p-th tile of rank r.
+ *    ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the
+ *    chunk's row tiles (ascending) are split into row groups of RG tiles
+ *    (RG <= 0: the whole chunk).  Each row group is one forward sweep over the
+ *    group's column tiles.  For each column tile a sweep takes the row group's
+ *    tiles in ascending order.
+ *  - seq == 0: the W ranks run side by side: entry p*W + r of the global order
+ *    is the p-th tile of rank r.  seq != 0: the ranks run one after another:
+ *    entry r*T + p (T = nM*nN tiles per rank) is the p-th tile of rank r.
  * Writes (r, mt, nt) triples to out[3*g .. 3*g+2].  Returns the number of
  * entries W*nM*nN, -1 on bad arguments, or -2 if cap (in entries) is too small.
  */
-int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int RG,
+int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int RG, int seq,
                         int32_t *out, int64_t cap)
 {
     if (W < 1 || M < 1 || N < 1 || BM < 1 || BN < 1 || M % W != 0)
@@ -245,7 +247,7 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int 
             return -1;
         }
         for (int64_t q = 0; q < T; ++q) {
-            const int64_t g = q * W + r;
+            const int64_t g = seq ? (int64_t)r * T + q : q * W + r;
             out[3 * g] = r;
             out[3 * g + 1] = list[2 * q];
             out[3 * g + 2] = list[2 * q + 1];

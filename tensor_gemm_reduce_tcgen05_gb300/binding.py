@@ -37,6 +37,9 @@ GEMM_RS_DEBUG_STALL_PRODUCER = 1
 
 GEMM_RS_REDUCE_CHAIN = 0
 GEMM_RS_REDUCE_LAST_ARRIVER = 1
+GEMM_RS_RANKS_DEFAULT = 0
+GEMM_RS_RANKS_SEQUENTIAL = 1
+GEMM_RS_RANKS_INTERLEAVED = 2
 
 _DTYPES = {"bf16": GEMM_RS_BF16, "fp32": GEMM_RS_FP32}
 
@@ -73,10 +76,10 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_last_error": (ctypes.c_char_p, []),
             "gemm_rs_status": (i32, [vp, vp]),
             "gemm_rs_reset": (i32, [vp, vp]),
-            "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, i32, i32, vp, i64]),
-            "gemm_rs_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 7),
+            "gemm_rs_schedule": (i64, [i64, i64, i32, i32, i32, i32, i32, i32, vp, i64]),
+            "gemm_rs_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 8),
             "gemm_rs_set_reduce_mode": (i32, [vp, i32]),
-            "gemm_rs_set_schedule": (i32, [vp, i32, i32]),
+            "gemm_rs_set_schedule": (i32, [vp, i32, i32, i32]),
             "gemm_rs_set_tile_n": (i32, [vp, i32]),
             "gemm_rs_set_tile": (i32, [vp, i32, i32]),
             "gemm_rs_set_timeout_cycles": (i32, [vp, u64]),
@@ -141,27 +144,27 @@ def gemm_rs_reset(h, stream=0) -> None:
 
 
 def gemm_rs_schedule(M: int, N: int, W: int, bm: int, bn: int, colgroup: int = 0,
-                     rowgroup: int = 0) -> np.ndarray:
+                     rowgroup: int = 0, rank_order: int = 0) -> np.ndarray:
     nM, nN = -(-M // bm), -(-N // bn)
     out = np.zeros((W * nM * nN, 3), dtype=np.int32)
-    n = _check(lib().gemm_rs_schedule(M, N, W, bm, bn, colgroup, rowgroup, out.ctypes.data,
-                                      out.shape[0]))
+    n = _check(lib().gemm_rs_schedule(M, N, W, bm, bn, colgroup, rowgroup, rank_order,
+                                      out.ctypes.data, out.shape[0]))
     return out[:n]
 
 
 def gemm_rs_get_plan(h) -> dict:
-    v = [ctypes.c_int() for _ in range(7)]
+    v = [ctypes.c_int() for _ in range(8)]
     _check(lib().gemm_rs_get_plan(h, *[ctypes.byref(x) for x in v]))
-    return dict(zip(("bm", "bn", "stages", "grid", "colgroup", "rowgroup", "reduce_mode"),
-                    (x.value for x in v)))
+    return dict(zip(("bm", "bn", "stages", "grid", "colgroup", "rowgroup", "rank_order",
+                     "reduce_mode"), (x.value for x in v)))
 
 
 def gemm_rs_set_reduce_mode(h, mode: int) -> None:
     _check(lib().gemm_rs_set_reduce_mode(h, mode))
 
 
-def gemm_rs_set_schedule(h, colgroup: int = 0, rowgroup: int = 0) -> None:
-    _check(lib().gemm_rs_set_schedule(h, colgroup, rowgroup))
+def gemm_rs_set_schedule(h, colgroup: int = 0, rowgroup: int = 0, rank_order: int = 0) -> None:
+    _check(lib().gemm_rs_set_schedule(h, colgroup, rowgroup, rank_order))
 
 
 def gemm_rs_set_tile_n(h, bn: int) -> None:

@@ -237,17 +237,18 @@ void pick_tile(int64_t M, int64_t N, int W, int sms, int *bm, int *bn)
 }
 
 // Row tiles per column sweep.  A sweep keeps its row tiles' A rows live in
-// L2 for every rank at once, so bound them to about 64 MB across the W ranks.
+// L2 for every live rank (1 when the ranks run one after another, W when they
+// run side by side), so bound them to about 64 MB across the live ranks.
 // Returns the chunk's row tile count (one sweep per step) when that fits.
-int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm)
+int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm, int live)
 {
     // row tiles keyed to one chunk: at most ceil(R/bm), plus one when R is ragged
     const int64_t R = M / W;
     const int64_t rows_per_chunk = cdiv(R, bm) + (R % bm != 0 ? 1 : 0);
-    const int64_t panel = static_cast<int64_t>(bm) * Kpr * 2 * W;
+    const int64_t panel = static_cast<int64_t>(bm) * Kpr * 2 * live;
     if (panel <= 0 || rows_per_chunk <= 1)
         return static_cast<int>(rows_per_chunk > 0 ? rows_per_chunk : 1);
-    // The A rows live across the W ranks' sweeps stay within about half of L2.
+    // The A rows live across the live ranks' sweeps stay within about half of L2.
     const int64_t budget = int64_t(64) << 20;
     int64_t rg = budget / panel;
     if (rg < 1)
@@ -262,12 +263,15 @@ int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm)
 // Column tiles per group when the caller leaves it to the library.  The model
 // counts the operand bytes read from DRAM.  With k column groups, the A rows
 // of every chunk are read once per group (k * |A|).  The B panels of one group
-// are read once if the W ranks' panels of a group fit in about 64 MB of L2,
+// are read once if the live ranks' panels of a group fit in about 64 MB of L2,
 // and once per step (W * |B|) otherwise.  k = 1, 2, 4, 8 are tried and the
-// least traffic wins (a tie keeps fewer groups).  A group must also hold
-// enough tiles that consecutive contributions to one output tile lie at least
-// 1.25 waves of workers apart, so that they arrive in step order.
-int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int64_t workers)
+// least traffic wins (a tie keeps fewer groups).  With the ranks side by side
+// (live = W), a group must also hold enough tiles that consecutive
+// contributions to one output tile lie at least 1.25 waves of workers apart,
+// so that they arrive in step order; one after another (live = 1), they are a
+// rank's pass apart whatever the group.
+int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int64_t workers,
+                  int live)
 {
     const int64_t nN = cdiv(N, bn);
     const int64_t nMs = cdiv(M, bm);
@@ -283,9 +287,9 @@ int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int6
             break;
         prev = G;
         const double sep = static_cast<double>(nMs) * G * (W - 1) / W; // work items apart
-        if (k > 1 && sep < 1.25 * static_cast<double>(workers))
+        if (k > 1 && live > 1 && sep < 1.25 * static_cast<double>(workers))
             break;
-        const double b_live = 2.0 * W * Kpr * G * bn;
+        const double b_live = 2.0 * live * Kpr * G * bn;
         const double cost = a_bytes * static_cast<double>(cdiv(nN, G)) + b_bytes * (b_live <= budget ? 1 : W);
         if (k == 1 || cost < best_cost) {
             best = G;
@@ -307,6 +311,7 @@ struct gemm_rs_s {
     int device, sms, pair_clusters, bm, bn;
     int colgroup; // 0: the default (pick_colgroup)
     int rowgroup; // 0: the default (pick_rowgroup)
+    int rank_order; // GEMM_RS_RANKS_*
     int reduce_mode; // GEMM_RS_REDUCE_CHAIN (default) or GEMM_RS_REDUCE_LAST_ARRIVER
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
@@ -325,12 +330,22 @@ int64_t workers_of(const gemm_rs_s *h)
     return total < cap ? total : cap;
 }
 
+bool sequential(const gemm_rs_s *h) { return h->rank_order != GEMM_RS_RANKS_INTERLEAVED; }
+
+// Ranks whose operands are live at once.
+int live_ranks(const gemm_rs_s *h) { return sequential(h) ? 1 : h->W; }
+
+int rowgroup_of(const gemm_rs_s *h)
+{
+    return h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm, live_ranks(h));
+}
+
 int colgroup_of(const gemm_rs_s *h)
 {
     const int64_t nN = cdiv(h->N, h->bn);
     if (h->colgroup > 0)
         return static_cast<int>(h->colgroup < nN ? h->colgroup : nN);
-    return pick_colgroup(h->M, h->N, h->Kpr, h->W, h->bm, h->bn, workers_of(h));
+    return pick_colgroup(h->M, h->N, h->Kpr, h->W, h->bm, h->bn, workers_of(h), live_ranks(h));
 }
 
 } // namespace
@@ -399,6 +414,7 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     pick_tile(M, N, W, sms, &h->bm, &h->bn);
     h->colgroup = 0;
     h->rowgroup = 0;
+    h->rank_order = GEMM_RS_RANKS_DEFAULT;
     h->reduce_mode = GEMM_RS_REDUCE_CHAIN;
     h->tmA_ptr = h->tmB_ptr = nullptr;
     h->timeout = 1ull << 32;
@@ -415,7 +431,7 @@ int gemm_rs_destroy(gemm_rs_t h)
 }
 
 int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int *colgroup,
-                     int *rowgroup, int *reduce_mode)
+                     int *rowgroup, int *rank_order, int *reduce_mode)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
@@ -429,7 +445,9 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int 
     if (colgroup)
         *colgroup = colgroup_of(h);
     if (rowgroup)
-        *rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
+        *rowgroup = rowgroup_of(h);
+    if (rank_order)
+        *rank_order = sequential(h) ? GEMM_RS_RANKS_SEQUENTIAL : GEMM_RS_RANKS_INTERLEAVED;
     if (reduce_mode)
         *reduce_mode = h->reduce_mode;
     if (grid) {
@@ -467,15 +485,18 @@ int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn)
     return GEMM_RS_OK;
 }
 
-int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup)
+int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup, int rank_order)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
     if (colgroup < 0 || rowgroup < 0)
         return fail(GEMM_RS_ERR_ARG, "column group %d / row group %d is negative", colgroup,
                     rowgroup);
+    if (rank_order < GEMM_RS_RANKS_DEFAULT || rank_order > GEMM_RS_RANKS_INTERLEAVED)
+        return fail(GEMM_RS_ERR_ARG, "unknown rank order %d", rank_order);
     h->colgroup = colgroup;
     h->rowgroup = rowgroup;
+    h->rank_order = rank_order;
     return GEMM_RS_OK;
 }
 
@@ -565,8 +586,9 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nK = static_cast<int>(cdiv(h->Kpr, gemm_rs::kBK));
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
     a.colgroup = colgroup_of(h);
-    a.rowgroup = h->rowgroup > 0 ? h->rowgroup : pick_rowgroup(h->M, h->Kpr, h->W, h->bm);
+    a.rowgroup = rowgroup_of(h);
     a.chain = h->reduce_mode == GEMM_RS_REDUCE_CHAIN ? 1 : 0;
+    a.seq = sequential(h) ? 1 : 0;
     a.R = h->M / h->W;
     a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
@@ -647,7 +669,7 @@ int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream)
 }
 
 int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgroup, int rowgroup,
-                         int32_t *out, int64_t cap)
+                         int rank_order, int32_t *out, int64_t cap)
 {
     if (W < 1 || W > 16)
         return fail(GEMM_RS_ERR_ARG, "W = %d is outside 1..16", W);
@@ -660,11 +682,14 @@ int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn, int colgro
     if (colgroup < 0 || rowgroup < 0)
         return fail(GEMM_RS_ERR_ARG, "column group %d / row group %d is negative", colgroup,
                     rowgroup);
+    if (rank_order < GEMM_RS_RANKS_DEFAULT || rank_order > GEMM_RS_RANKS_INTERLEAVED)
+        return fail(GEMM_RS_ERR_ARG, "unknown rank order %d", rank_order);
     const int nN = static_cast<int>(cdiv(N, bn));
     const int nMs = static_cast<int>(cdiv(M, bm));
     const gemm_rs::Sched s{W, nMs, nN, bm == gemm_rs::kBM ? 7 : 8, M / W,
                            (colgroup == 0 || colgroup > nN) ? nN : colgroup,
-                           rowgroup == 0 ? nMs : rowgroup};
+                           rowgroup == 0 ? nMs : rowgroup,
+                           rank_order == GEMM_RS_RANKS_INTERLEAVED ? 0 : 1};
     const int64_t total = static_cast<int64_t>(W) * s.nM * s.nN;
     if (cap < total)
         return fail(GEMM_RS_ERR_SHAPE, "cap %lld < %lld entries", (long long)cap, (long long)total);
@@ -831,6 +856,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.colgroup = a.nN;
     a.rowgroup = a.nM;
     a.chain = 1;
+    a.seq = 1;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

@@ -111,6 +111,7 @@ struct KernelArgs {
     int colgroup;   // column tiles per schedule group (>= nN: one group)
     int rowgroup;   // row tiles per sweep (>= a chunk's row tiles: one sweep per step)
     int chain;      // 1: chain reduction (in-order fold as tiles land), 0: last arriver reduces
+    int seq;        // 1: the ranks' tiles one rank after another, 0: the ranks side by side
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -415,8 +416,10 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
 //   bits  0-15  positions whose partial is stored in their slot and not yet folded
 //   bits 16-20  k: positions 0 .. k-1 are folded; their running sum is in slot 0
 //   bit  24     owned: one CTA is folding from position k on
-// Position i is the step in which its rank reaches the tile, so in a steady run
-// the positions arrive in order and each one folds itself straight from TMEM.
+// Position i is the contribution's place in the tile's arrival order (the step
+// in which its rank reaches the tile, or the rank itself when the ranks run one
+// after another), so in a steady run the positions arrive in order and each one
+// folds itself straight from TMEM.
 // The flag's release/acquire chain orders the folds: position i's additions
 // to slot 0 all happen before position i+1's, so every element is summed in
 // position order, the same order on every run.
@@ -523,15 +526,16 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
 // Last-arriver mode: every rank stores its partial in slot r, counts itself in
 // on the tile's counter, and the rank that arrives last queues the tile: the
 // consumers fold slots 0 .. W-1 (rank order) into Y.
-// Chain mode: the rank at position i (its step) folds its own partial straight
-// from TMEM onto the running sum in slot 0 when positions 0 .. i-1 are done:
-// position 0 stores it, positions 1 .. W-2 add to it in L2 (red.add, nothing
-// comes back to the SM), and the last position reads it and writes Y.  A rank
-// that is early stores its partial in slot i.  Whoever owns the fold when the positions after it are
-// already stored (or the early rank itself, once its turn has come) folds
-// them from their slots.  The chain mode has no reduce jobs, so warps 6-9 join
-// the epilogue: two warps per TMEM lane quarter, each draining half of the
-// tile's 32-column slabs.
+// Chain mode: the rank at position i (the tile's arrival order: its step when
+// the ranks run side by side, its rank when they run one after another) folds
+// its own partial straight from TMEM onto the running sum in slot 0 when
+// positions 0 .. i-1 are done: position 0 stores it, positions 1 .. W-2 add to
+// it in L2 (red.add, nothing comes back to the SM), and the last position reads
+// it and writes Y.  A rank that is early stores its partial in slot i.
+// Whoever owns the fold when the positions after it are already stored (or
+// the early rank itself, once its turn has come) folds them from their slots.
+// The chain mode has no reduce jobs, so warps 6-9 join the epilogue: two warps
+// per TMEM lane quarter, each draining half of the tile's 32-column slabs.
 template <int BN, bool PAIR>
 __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &sch, uint32_t tmem,
                                              SmemCtl *ctl, int warp, int lane, int64_t g0,
@@ -555,8 +559,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     uint32_t rq_n = 0;
     int it = 0;
     for (int64_t g = g0; g < a.total; g += gstride, ++it) {
-        int r, mts, nt, step;
-        decode_tile(sch, g, r, mts, nt, step);
+        int r, mts, nt, pos;
+        decode_tile(sch, g, r, mts, nt, pos);
         const int mt = PAIR ? 2 * mts + static_cast<int>(crank) : mts;
         const bool half_ok = mt < a.nM; // a pair's second half may lie wholly below M
         const int tile = mt * a.nN + nt;
@@ -565,18 +569,18 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         // computed, so the decision is ready when it lands.
         if (etid == 0)
             ctl->epi_direct[buf] =
-                (a.chain && half_ok && chain_try_own(a.flags + tile, static_cast<uint32_t>(step))) ? 1 : 0;
+                (a.chain && half_ok && chain_try_own(a.flags + tile, static_cast<uint32_t>(pos))) ? 1 : 0;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
         const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
                                  : ptx::mbar_wait(fb, aph, a.timeout, abort_flag);
-        // If position step-1 was not folded yet at the start, wait a little for
+        // If position pos-1 was not folded yet at the start, wait a little for
         // it now that the accumulator has landed: a store and a later fold
         // cost far more.  Late positions come mostly from the first step of a
         // column group, whose B panels are not in L2 yet.
         if (etid == 0 && a.chain && waited && half_ok && ctl->epi_direct[buf] == 0)
             ctl->epi_direct[buf] =
-                chain_wait_own(a.flags + tile, static_cast<uint32_t>(step), kChainWaitCycles) ? 1 : 0;
+                chain_wait_own(a.flags + tile, static_cast<uint32_t>(pos), kChainWaitCycles) ? 1 : 0;
         if (ptx::named_bar_or(kBarEpi, nthr, !(waited && ok))) {
             ok = false;
             break;
@@ -597,10 +601,10 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         // Chain mode: the running sum lives in slot 0.  Position 0 stores it,
         // positions 1 .. W-2 add to it in L2, and the last position reads it
         // and writes Y.  An early position stores its partial in its own slot.
-        const int sidx = a.chain ? (direct ? 0 : step) : r;  // slot written
-        const bool to_y = direct && step == a.W - 1;         // the last fold writes Y
-        const bool add_prev = to_y && step > 0;              // read the running sum
-        const bool add_l2 = direct && step > 0 && !to_y;     // add to it in L2
+        const int sidx = a.chain ? (direct ? 0 : pos) : r; // slot written
+        const bool to_y = direct && pos == a.W - 1;        // the last fold writes Y
+        const bool add_prev = to_y && pos > 0;             // read the running sum
+        const bool add_l2 = direct && pos > 0 && !to_y;    // add to it in L2
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
@@ -723,14 +727,14 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 if (direct) {
                     if (to_y)
                         ptx::st_relaxed_gpu(flag, 0u); // back to 0 for the next call
-                    else if (chain_pass_on(flag, static_cast<uint32_t>(step + 1),
-                                           (static_cast<uint32_t>(step) << 16) | kChainOwn))
-                        fold_from = step + 1;
+                    else if (chain_pass_on(flag, static_cast<uint32_t>(pos + 1),
+                                           (static_cast<uint32_t>(pos) << 16) | kChainOwn))
+                        fold_from = pos + 1;
                 } else {
-                    const uint32_t old = ptx::atom_or_acq_rel_gpu(flag, 1u << step);
-                    if (chain_k(old) == static_cast<uint32_t>(step) && !(old & kChainOwn) &&
-                        chain_try_own(flag, static_cast<uint32_t>(step)))
-                        fold_from = step;
+                    const uint32_t old = ptx::atom_or_acq_rel_gpu(flag, 1u << pos);
+                    if (chain_k(old) == static_cast<uint32_t>(pos) && !(old & kChainOwn) &&
+                        chain_try_own(flag, static_cast<uint32_t>(pos)))
+                        fold_from = pos;
                 }
                 ctl->epi_fold = fold_from;
             }
@@ -824,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const Sched sch{a.W, a.nMs, a.nN, 7, a.R, a.colgroup, a.rowgroup};
+    const Sched sch{a.W, a.nMs, a.nN, 7, a.R, a.colgroup, a.rowgroup, a.seq};
 
     if (warp == 0) {
         if (lane == 0)
@@ -1051,7 +1055,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cluster_sync(); // the peer's barriers are initialised before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
-    const Sched sch{a.W, a.nMs, a.nN, 8, a.R, a.colgroup, a.rowgroup};
+    const Sched sch{a.W, a.nMs, a.nN, 8, a.R, a.colgroup, a.rowgroup, a.seq};
 
     if (warp == 0) {
         if (lane == 0)

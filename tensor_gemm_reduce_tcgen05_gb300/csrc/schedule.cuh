@@ -20,11 +20,22 @@
 // ((W-r) mod W)*gn/W and wraps around within the group, so all ranks cover
 // the same columns in a group and each B panel of the group stays in use for
 // all W steps.  Row groups bound the A rows a sweep keeps live, so they can
-// stay in L2 while the columns go by.  The ranks advance side by side: global
-// entry g is rank (g mod W)'s (g / W)-th tile.  Every sweep runs forward, and
-// the rank that reaches a tile at step s+1 (rank r-1) starts its sweep gn/W
-// columns earlier than rank r: it reaches the tile between 1 - 1/W and about
-// 2 steps after rank r did, so a tile's contributions arrive in step order.
+// stay in L2 while the columns go by.
+//
+// Two rank orders:
+//   interleaved  the ranks advance side by side: global entry g is rank
+//                (g mod W)'s (g / W)-th tile, so at every step the W ranks
+//                target W different chunks.  Every sweep runs forward, and the
+//                rank that reaches a tile at step s+1 (rank r-1) starts its
+//                sweep gn/W columns earlier than rank r: it reaches the tile
+//                between 1 - 1/W and about 2 steps after rank r did, so a
+//                tile's contributions arrive in step order.
+//   sequential   the ranks run one after another: global entry g is rank
+//                (g / T)'s (g mod T)-th tile, T = nM*nN.  One rank's operands
+//                are live at a time, and a tile's contributions arrive in rank
+//                order, most of a rank's pass apart.
+// The chain reduction folds a tile's contributions in that arrival order, its
+// "position": the step (interleaved) or the rank (sequential).
 #pragma once
 
 #include <cstdint>
@@ -38,6 +49,7 @@ struct Sched {
     int64_t R;    // rows per chunk, M / W
     int G;        // column tiles per group (>= nN: one group)
     int RG;       // row tiles per row group (>= a chunk's row tiles: one group)
+    int seq;      // 1: ranks one after another, 0: ranks side by side
 };
 
 __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
@@ -45,13 +57,21 @@ __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
     return (x + (int64_t(1) << s) - 1) >> s;
 }
 
-// Decode global entry g into (r, mt, nt) and the step (0 .. W-1) in which rank
-// r reaches the tile's chunk.  g must be < W*nM*nN.
+// Decode global entry g into (r, mt, nt) and the tile's position (0 .. W-1)
+// in its contributions' arrival order: the step in which rank r reaches the
+// tile's chunk (interleaved), or r (sequential).  g must be < W*nM*nN.
 __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
-                                                     int &nt, int &step)
+                                                     int &nt, int &pos)
 {
-    r = static_cast<int>(g % s.W);
-    int64_t p = g / s.W;
+    int64_t p;
+    if (s.seq) {
+        const int64_t T = static_cast<int64_t>(s.nM) * s.nN;
+        r = static_cast<int>(g / T);
+        p = g - static_cast<int64_t>(r) * T;
+    } else {
+        r = static_cast<int>(g % s.W);
+        p = g / s.W;
+    }
     const int64_t G = s.G < s.nN ? s.G : s.nN;
     // Every group but the last is full, so the group index follows directly.
     const int64_t grp = p / (G * s.nM);
@@ -82,21 +102,21 @@ __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, 
             if (n >= gn)
                 n -= gn;
             nt = static_cast<int>(g0 + n);
-            step = st;
+            pos = s.seq ? r : st;
             return;
         }
         p -= items;
     }
     mt = -1;
     nt = -1;
-    step = -1;
+    pos = -1;
 }
 
 __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
                                                      int &nt)
 {
-    int step;
-    decode_tile(s, g, r, mt, nt, step);
+    int pos;
+    decode_tile(s, g, r, mt, nt, pos);
 }
 
 } // namespace gemm_rs

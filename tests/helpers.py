@@ -50,7 +50,7 @@ def assert_close(y_gpu: np.ndarray, y_ref: np.ndarray, y_dtype: str, what: str =
 
 
 def run_gpu(A, B, C, W, M, N, Kpr, alpha, beta, y_dtype, tile_n=None, calls=1, poison=False,
-            tile_m=None, reduce_mode=None):
+            tile_m=None, reduce_mode=None, rank_order=None):
     """Run the fused path through the C ABI.  Returns (Y as numpy, plan, op)."""
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
     dev = torch.device("cuda", 0)
@@ -58,6 +58,8 @@ def run_gpu(A, B, C, W, M, N, Kpr, alpha, beta, y_dtype, tile_n=None, calls=1, p
                   tile_m=tile_m)
     if reduce_mode is not None:
         b.gemm_rs_set_reduce_mode(op.handle, reduce_mode)
+    if rank_order is not None:
+        b.gemm_rs_set_schedule(op.handle, 0, 0, rank_order)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = None if C is None else C.to(dev)
     Y = op.new_output()

@@ -51,13 +51,16 @@ def test_version(b):
     (16, 16 * 7, 64, 64), (7, 7 * 129, 264, 128),
 ])
 def test_schedule_matches_oracle(b, W, M, N, bn):
+    orders = ((b.GEMM_RS_RANKS_INTERLEAVED, "interleaved"), (b.GEMM_RS_RANKS_SEQUENTIAL, "sequential"),
+              (b.GEMM_RS_RANKS_DEFAULT, "sequential"))
     for G, RG in ((0, 0), (1, 0), (2, 3), (5, 1), (0, 2), (3, 5)):
-        ours = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG)
-        ref = oracle.schedule(W, M, N, 128, bn, G, RG)
-        np.testing.assert_array_equal(ours, ref)
-        # the CTA-pair kernel walks 256-row tiles
-        np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256, G, RG),
-                                      oracle.schedule(W, M, N, 256, 256, G, RG))
+        for code, order in orders:
+            ours = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG, code)
+            ref = oracle.schedule(W, M, N, 128, bn, G, RG, order)
+            np.testing.assert_array_equal(ours, ref)
+            # the CTA-pair kernel walks 256-row tiles
+            np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256, G, RG, code),
+                                          oracle.schedule(W, M, N, 256, 256, G, RG, order))
 
 
 def test_workspace_bytes(b):
@@ -112,6 +115,8 @@ def test_null_handle_calls_fail_cleanly(b):
         b.gemm_rs_schedule(255, 256, 2, 128, 256)
     with pytest.raises(b.GemmRSError):
         b.gemm_rs_schedule(256, 256, 2, 64, 256)
+    with pytest.raises(b.GemmRSError):
+        b.gemm_rs_schedule(256, 256, 2, 128, 256, 0, 0, 3)  # unknown rank order
 
 
 def test_reduce_partials_validates(b):

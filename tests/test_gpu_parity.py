@@ -34,14 +34,19 @@ TILES = [(128, 256), (128, 128), (128, 64), (256, 256)]  # (256, 256): the CTA-p
 MODES = [0, 1]  # GEMM_RS_REDUCE_CHAIN, GEMM_RS_REDUCE_LAST_ARRIVER
 
 
+ORDERS = [1, 2]  # GEMM_RS_RANKS_SEQUENTIAL (the default), GEMM_RS_RANKS_INTERLEAVED
+
+
+@pytest.mark.parametrize("order", ORDERS)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
-def test_integer_inputs_bit_exact(W, M, N, Kpr, tile, mode):
+def test_integer_inputs_bit_exact(W, M, N, Kpr, tile, mode, order):
     A, B, _ = inputs(W, M, N, Kpr, "int")
     y, plan, op = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
-                          tile_n=tile[1], reduce_mode=mode)
-    assert (plan["bm"], plan["bn"], plan["reduce_mode"]) == (tile[0], tile[1], mode)
+                          tile_n=tile[1], reduce_mode=mode, rank_order=order)
+    assert (plan["bm"], plan["bn"], plan["reduce_mode"], plan["rank_order"]) == \
+        (tile[0], tile[1], mode, order)
     assert int(op.flags_view().abs().sum()) == 0
     ref = oracle_y(A, B, None, 1.0, 0.0, "fp32")
     np.testing.assert_array_equal(y, ref)
@@ -58,12 +63,14 @@ def test_integer_inputs_with_c_bit_exact(W, M, N, Kpr, tile):
         np.testing.assert_array_equal(y, ref)
 
 
+@pytest.mark.parametrize("order", ORDERS)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("W,M,N,Kpr", SHAPES)
 @pytest.mark.parametrize("y_dtype", ["fp32", "bf16"])
-def test_normal_inputs_within_tolerance(W, M, N, Kpr, y_dtype, mode):
+def test_normal_inputs_within_tolerance(W, M, N, Kpr, y_dtype, mode, order):
     A, B, C = inputs(W, M, N, Kpr, "normal", c_dist="normal1")
-    y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype, reduce_mode=mode)
+    y, _, _ = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, y_dtype, reduce_mode=mode,
+                      rank_order=order)
     assert_close(y, oracle_y(A, B, C, 0.5, 1.0, y_dtype), y_dtype, f"{(W, M, N, Kpr)}")
 
 
@@ -81,9 +88,11 @@ def test_nan_poisoned_workspace_and_output():
     A, B, _ = inputs(W, M, N, Kpr, "int")
     for tile in ((128, 256), (128, 64), (256, 256)):
         for mode in MODES:
-            y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
-                              tile_n=tile[1], poison=True, reduce_mode=mode)
-        np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+            for order in ORDERS:
+                y, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", tile_m=tile[0],
+                                  tile_n=tile[1], poison=True, reduce_mode=mode,
+                                  rank_order=order)
+                np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
 def test_beta_zero_ignores_nan_c():
@@ -138,16 +147,19 @@ def test_twenty_calls_bit_identical_and_counters_reset(mode):
 
 def test_device_schedule_record_matches_schedule_and_oracle():
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
-    for (W, M, N, Kpr, bm, bn, G, RG) in [(8, 1024, 1024, 64, 128, 256, 0, 0),
-                                          (3, 300, 520, 64, 128, 128, 2, 1),
-                                          (8, 64, 8192, 64, 128, 64, 0, 0),
-                                          (8, 4096, 1024, 64, 256, 256, 0, 0),
-                                          (8, 4096, 2048, 64, 256, 256, 3, 1),
-                                          (4, 4096, 2048, 64, 256, 256, 0, 3),
-                                          (3, 300, 520, 64, 256, 256, 1, 0)]:
+    for (W, M, N, Kpr, bm, bn, G, RG, ro) in [(8, 1024, 1024, 64, 128, 256, 0, 0, 0),
+                                              (8, 1024, 1024, 64, 128, 256, 0, 0, 2),
+                                              (3, 300, 520, 64, 128, 128, 2, 1, 2),
+                                              (3, 300, 520, 64, 128, 128, 2, 1, 1),
+                                              (8, 64, 8192, 64, 128, 64, 0, 0, 0),
+                                              (8, 4096, 1024, 64, 256, 256, 0, 0, 2),
+                                              (8, 4096, 1024, 64, 256, 256, 0, 0, 1),
+                                              (8, 4096, 2048, 64, 256, 256, 3, 1, 2),
+                                              (4, 4096, 2048, 64, 256, 256, 0, 3, 0),
+                                              (3, 300, 520, 64, 256, 256, 1, 0, 2)]:
         A, B, _ = inputs(W, M, N, Kpr, "int")
         op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_m=bm, tile_n=bn)
-        b.gemm_rs_set_schedule(op.handle, G, RG)
+        b.gemm_rs_set_schedule(op.handle, G, RG, ro)
         nM, nN = -(-M // bm), -(-N // bn)
         rec = torch.full((W * nM * nN, 4), -1, dtype=torch.int32, device="cuda:0")
         b.gemm_rs_set_debug(op.handle, rec.data_ptr(), 0)
@@ -155,11 +167,15 @@ def test_device_schedule_record_matches_schedule_and_oracle():
         torch.cuda.synchronize()
         rec = rec.cpu().numpy()
         plan = op.plan
-        lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn, plan["colgroup"], plan["rowgroup"])
+        assert plan["rank_order"] == (b.GEMM_RS_RANKS_INTERLEAVED if ro == 2
+                                      else b.GEMM_RS_RANKS_SEQUENTIAL)
+        order = "interleaved" if ro == 2 else "sequential"
+        lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn, plan["colgroup"], plan["rowgroup"],
+                                       plan["rank_order"])
         np.testing.assert_array_equal(rec[:, :3], lib_sched)
         np.testing.assert_array_equal(rec[:, :3],
                                       oracle.schedule(W, M, N, bm, bn, plan["colgroup"],
-                                                      plan["rowgroup"]))
+                                                      plan["rowgroup"], order))
         grid = op.plan["grid"]
         workers = grid // 2 if bm == 256 else grid  # CTA pairs process one entry each
         np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % workers)
@@ -192,19 +208,25 @@ def test_timeout_path_reports_and_recovers(tile):
 
 
 def test_reduce_modes_agree_and_each_is_deterministic():
-    """Both reductions on one shape with many tiles per chunk: each is bit-identical
-    across calls, and the two agree within the fp32 tolerance (they differ only in
-    summation order)."""
+    """Both reductions and both rank orders on one shape with many tiles per
+    chunk: each is bit-identical across calls, and all agree within the fp32
+    tolerance (they differ only in summation order).  With the ranks one after
+    another, the chain folds in rank order, the last arriver's order."""
     W, M, N, Kpr = 8, 2048, 1536, 512
     A, B, _ = inputs(W, M, N, Kpr, "normal")
     outs = {}
     for mode in MODES:
-        y1, _, op = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode, calls=3)
-        y2, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode)
-        np.testing.assert_array_equal(y1, y2)
-        outs[mode] = y1
-    assert_close(outs[0], outs[1], "fp32", "chain vs last arriver")
-    assert_close(outs[0], oracle_y(A, B, None, 1.0, 0.0, "fp32"), "fp32", "chain vs oracle")
+        for order in ORDERS:
+            y1, _, op = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode,
+                                calls=3, rank_order=order)
+            y2, _, _ = run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=mode,
+                               rank_order=order)
+            np.testing.assert_array_equal(y1, y2)
+            outs[mode, order] = y1
+    ref = oracle_y(A, B, None, 1.0, 0.0, "fp32")
+    for key, y in outs.items():
+        assert_close(y, outs[1, 1], "fp32", f"{key} vs last arriver")
+        assert_close(y, ref, "fp32", f"{key} vs oracle")
 
 
 def test_baseline_reduce_kernel_matches_oracle():
@@ -224,10 +246,11 @@ def test_baseline_reduce_kernel_matches_oracle():
         np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, C, 0.5, 1.0, y_dtype))
 
 
+@pytest.mark.parametrize("order", ORDERS)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["ffn_w8_m4096", "ffn_w8_m8192_bias", "decode_w8_m64",
                                   "ffn_w4_m16384_x20"])
-def test_full_size_workloads_on_row_sample(name, mode):
+def test_full_size_workloads_on_row_sample(name, mode, order):
     """The full-size workloads in the launch configuration the benchmark
     times, checked on a row sample: every chunk's first and last row, four
     row-tile boundaries (both rows at each), and 8 seeded random rows.  The
@@ -235,7 +258,7 @@ def test_full_size_workloads_on_row_sample(name, mode):
     w = WORKLOADS[name]
     A, B, C = workload_inputs(w)
     y, plan, op = run_gpu(A, B, C, w.W, w.M, w.N, w.Kpr, w.alpha, w.beta, w.y_dtype,
-                          calls=w.calls, reduce_mode=mode)
+                          calls=w.calls, reduce_mode=mode, rank_order=order)
     rows = sample_rows(w.M, w.W, n_random=8, n_boundaries=4)
     ref = oracle_y(A, B, C, w.alpha, w.beta, w.y_dtype, rows=rows)
     assert_close(y[rows], ref, w.y_dtype, name)

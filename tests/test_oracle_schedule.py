@@ -52,22 +52,30 @@ def test_matches_printed_rank_offset_order():
         assert [seq[-1]] + seq[:-1] == order      # = printed order, local moved to the front
 
 
+@pytest.mark.parametrize("order", ["interleaved", "sequential"])
 @pytest.mark.parametrize("G,RG", [(0, 0), (1, 0), (3, 0), (0, 1), (2, 3)])
 @pytest.mark.parametrize("W,M,N,BM,BN", [
     (2, 256, 256, 128, 256), (8, 4096, 4096, 128, 256), (4, 16384, 5120, 128, 256),
     (8, 64, 8192, 128, 64), (3, 300, 520, 128, 128), (1, 200, 72, 128, 64),
     (5, 5 * 128, 1000, 128, 256), (8, 4096, 4096, 256, 256),
 ])
-def test_schedule_properties(W, M, N, BM, BN, G, RG):
-    sched = oracle.schedule(W, M, N, BM, BN, G, RG)
+def test_schedule_properties(W, M, N, BM, BN, G, RG, order):
+    sched = oracle.schedule(W, M, N, BM, BN, G, RG, order)
     nM, nN = -(-M // BM), -(-N // BN)
     assert sched.shape == (W * nM * nN, 3)
     # every rank-tile exactly once
     keys = set(map(tuple, sched.tolist()))
     assert len(keys) == W * nM * nN
     assert keys == {(r, m, n) for r in range(W) for m in range(nM) for n in range(nN)}
-    # ranks run side by side
-    assert np.array_equal(sched[:, 0], np.tile(np.arange(W), nM * nN))
+    if order == "interleaved":
+        # ranks run side by side
+        assert np.array_equal(sched[:, 0], np.tile(np.arange(W), nM * nN))
+    else:
+        # one rank after another, each rank's own order unchanged
+        assert np.array_equal(sched[:, 0], np.repeat(np.arange(W), nM * nN))
+        side = oracle.schedule(W, M, N, BM, BN, G, RG, "interleaved")
+        for r in range(W):
+            assert np.array_equal(sched[sched[:, 0] == r], side[side[:, 0] == r])
     R = M // W
     groups = 1 if G <= 0 or G >= nN else -(-nN // G)
     for r in range(W):
@@ -78,7 +86,7 @@ def test_schedule_properties(W, M, N, BM, BN, G, RG):
             assert seq == expect
         else:
             assert seq == expect * groups  # remote chunks first, local last, in every group
-    if R % BM == 0:
+    if R % BM == 0 and order == "interleaved":
         # every position p: the W ranks target W distinct chunks
         per_p = sched.reshape(nM * nN, W, 3)
         for p in range(nM * nN):
@@ -141,6 +149,28 @@ def test_tile_contributions_arrive_in_step_order(W, M, N, BM, BN, G):
         per_step = nM * min(group, nN - g0)          # global entries per step of this group
         gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
         assert min(gaps) >= per_step * (W - 1) // W - W  # ranks interleave: -1 per rank
+
+
+@pytest.mark.parametrize("W,M,N,BM,BN,G", [
+    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
+    (8, 4096, 4096, 256, 256, 8), (3, 300, 520, 128, 128, 0), (5, 5 * 256, 1000, 128, 256, 2)])
+def test_sequential_ranks_arrive_in_rank_order(W, M, N, BM, BN, G):
+    """With the ranks one after another, every output tile sees its W rank
+    contributions in rank order 0 .. W-1 (the order the chain reduction folds
+    in, the same as the last arriver's).  Rank r+1 reaches a tile at most one
+    of its steps (T/W entries) earlier in its own pass than rank r, give or take
+    the column offset, so consecutive contributions lie at least T*(W-2)/W
+    entries apart (T = tiles per rank)."""
+    sched = oracle.schedule(W, M, N, BM, BN, G, 0, "sequential")
+    nM, nN = -(-M // BM), -(-N // BN)
+    T = nM * nN
+    seen = {}
+    for g, (r, mt, nt) in enumerate(sched.tolist()):
+        seen.setdefault((mt, nt), []).append((g, r))
+    for lst in seen.values():
+        assert [r for _, r in lst] == list(range(W))
+        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
+        assert min(gaps) >= T * (W - 2) // W
 
 
 def test_rank_column_offset_when_one_chunk_holds_all_tiles():
