@@ -247,11 +247,13 @@ GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
 /* Schedule (see gemm_rs_schedule).  "Live ranks" below is 1 for the
  * sequential rank order and W for the interleaved one.
  *   colgroup    column tiles per column group.  0 (the default) = the
- *               library's choice: 1, 2, 4 or 8 groups, whichever a model of
- *               the operand bytes read from DRAM favours (A rows are read once
- *               per group; a group's B panels of the live ranks are read once
- *               when they fit in about 64 MB, else once per step); with the
- *               ranks side by side, groups stay large enough that a tile's
+ *               library's choice.  Ranks one after another: two groups when
+ *               that keeps a group's fp32 running sums (M x its columns)
+ *               within 40 MB, else one.  Ranks side by side: 1, 2, 4 or 8
+ *               groups, whichever a model of the operand bytes read from DRAM
+ *               favours (A rows are read once per group; a group's B panels of
+ *               the W ranks are read once when they fit in about 64 MB, else
+ *               once per step), keeping groups large enough that a tile's
  *               contributions arrive in step order.
  *   rowgroup    row tiles per column sweep.  0 (the default) = the library's
  *               choice: the chunk's row tiles in the fewest groups of

@@ -191,8 +191,10 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
  *    group's column tiles.  For each column tile a sweep takes the row group's
  *    tiles in ascending order.
  *  - seq == 0: the W ranks run side by side: entry p*W + r of the global order
- *    is the p-th tile of rank r.  seq != 0: the ranks run one after another:
- *    entry r*T + p (T = nM*nN tiles per rank) is the p-th tile of rank r.
+ *    is the p-th tile of rank r.  seq != 0: for each column group in turn, the
+ *    ranks run one after another: the group's block of the global order holds
+ *    rank 0's tiles of the group (its nM*gn entries in its own order), then
+ *    rank 1's, and so on.
  * Writes (r, mt, nt) triples to out[3*g .. 3*g+2].  Returns the number of
  * entries W*nM*nN, -1 on bad arguments, or -2 if cap (in entries) is too small.
  */
@@ -247,7 +249,12 @@ int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int 
             return -1;
         }
         for (int64_t q = 0; q < T; ++q) {
-            const int64_t g = seq ? (int64_t)r * T + q : q * W + r;
+            int64_t g = q * W + r;
+            if (seq) {
+                const int64_t k = q / (nM * group);            /* column group of entry q */
+                const int64_t gn = (nN - k * group < group) ? nN - k * group : group;
+                g = k * W * nM * group + r * nM * gn + (q - k * nM * group);
+            }
             out[3 * g] = r;
             out[3 * g + 1] = list[2 * q];
             out[3 * g + 2] = list[2 * q + 1];

@@ -260,21 +260,37 @@ int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm, int live)
     return static_cast<int>(cdiv(rows_per_chunk, groups));
 }
 
-// Column tiles per group when the caller leaves it to the library.  The model
-// counts the operand bytes read from DRAM.  With k column groups, the A rows
-// of every chunk are read once per group (k * |A|).  The B panels of one group
-// are read once if the live ranks' panels of a group fit in about 64 MB of L2,
-// and once per step (W * |B|) otherwise.  k = 1, 2, 4, 8 are tried and the
-// least traffic wins (a tie keeps fewer groups).  With the ranks side by side
-// (live = W), a group must also hold enough tiles that consecutive
+// Column tiles per group when the caller leaves it to the library.
+//
+// Ranks side by side (live = W): the model counts the operand bytes read from
+// DRAM.  With k column groups, the A rows of every chunk are read once per
+// group (k * |A|).  The B panels of one group are read once if the W ranks'
+// panels of a group fit in about 64 MB of L2, and once per step (W * |B|)
+// otherwise.  k = 1, 2, 4, 8 are tried and the least traffic wins (a tie keeps
+// fewer groups).  A group must also hold enough tiles that consecutive
 // contributions to one output tile lie at least 1.25 waves of workers apart,
-// so that they arrive in step order; one after another (live = 1), they are a
-// rank's pass apart whatever the group.
+// so that they arrive in step order.
+//
+// Ranks one after another (live = 1): one rank's operands stay in L2 through
+// its pass whatever the group, but the running sums of a group (M x its
+// columns, fp32) stay live across all W passes.  Two groups are used when
+// that halves them to at most 40 MB, so that they stay in L2 for the price of
+// reading A twice, and when a rank's pass over half the columns still keeps a
+// tile's consecutive contributions 1.25 waves apart; otherwise one group.
 int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int64_t workers,
                   int live)
 {
     const int64_t nN = cdiv(N, bn);
     const int64_t nMs = cdiv(M, bm);
+    if (live == 1) {
+        const int64_t half = cdiv(nN, 2);
+        const double rs_half = 4.0 * static_cast<double>(M) * half * bn;
+        // consecutive ranks' contributions to a tile: about nMs*G*(W-2)/W items apart
+        const double sep = static_cast<double>(nMs) * half * (W - 2) / W;
+        const bool split = nN > 1 && rs_half <= 40.0 * (1 << 20) &&
+                           sep >= 1.25 * static_cast<double>(workers);
+        return static_cast<int>(split ? half : nN);
+    }
     const double a_bytes = 2.0 * W * M * Kpr;
     const double b_bytes = 2.0 * W * Kpr * N;
     const double budget = 64.0 * (1 << 20);
@@ -287,7 +303,7 @@ int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int6
             break;
         prev = G;
         const double sep = static_cast<double>(nMs) * G * (W - 1) / W; // work items apart
-        if (k > 1 && live > 1 && sep < 1.25 * static_cast<double>(workers))
+        if (k > 1 && sep < 1.25 * static_cast<double>(workers))
             break;
         const double b_live = 2.0 * live * Kpr * G * bn;
         const double cost = a_bytes * static_cast<double>(cdiv(nN, G)) + b_bytes * (b_live <= budget ? 1 : W);

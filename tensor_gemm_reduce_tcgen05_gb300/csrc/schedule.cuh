@@ -30,10 +30,11 @@
 //                sweep gn/W columns earlier than rank r: it reaches the tile
 //                between 1 - 1/W and about 2 steps after rank r did, so a
 //                tile's contributions arrive in step order.
-//   sequential   the ranks run one after another: global entry g is rank
-//                (g / T)'s (g mod T)-th tile, T = nM*nN.  One rank's operands
-//                are live at a time, and a tile's contributions arrive in rank
-//                order, most of a rank's pass apart.
+//   sequential   for each column group, the ranks run one after another: the
+//                group's entries are rank 0's tiles of the group, then rank
+//                1's, and so on.  One rank's operands and one group's running
+//                sums are live at a time, and a tile's contributions arrive in
+//                rank order, most of a rank's pass over the group apart.
 // The chain reduction folds a tile's contributions in that arrival order, its
 // "position": the step (interleaved) or the rank (sequential).
 #pragma once
@@ -63,19 +64,24 @@ __host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
 __host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
                                                      int &nt, int &pos)
 {
-    int64_t p;
+    const int64_t G = s.G < s.nN ? s.G : s.nN;
+    // Every column group but the last is full, so the group index follows
+    // directly.  p becomes rank r's index inside the group.
+    int64_t p, grp;
     if (s.seq) {
-        const int64_t T = static_cast<int64_t>(s.nM) * s.nN;
-        r = static_cast<int>(g / T);
-        p = g - static_cast<int64_t>(r) * T;
+        const int64_t full = static_cast<int64_t>(s.W) * s.nM * G; // entries of a full group
+        grp = g / full;
+        const int64_t gn = (s.nN - grp * G) < G ? (s.nN - grp * G) : G;
+        const int64_t q = g - grp * full;
+        const int64_t per_rank = static_cast<int64_t>(s.nM) * gn;
+        r = static_cast<int>(q / per_rank);
+        p = q - static_cast<int64_t>(r) * per_rank;
     } else {
         r = static_cast<int>(g % s.W);
         p = g / s.W;
+        grp = p / (G * s.nM);
+        p -= grp * G * s.nM;
     }
-    const int64_t G = s.G < s.nN ? s.G : s.nN;
-    // Every group but the last is full, so the group index follows directly.
-    const int64_t grp = p / (G * s.nM);
-    p -= grp * G * s.nM;
     const int64_t g0 = grp * G;
     const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
     const int64_t rot = (static_cast<int64_t>((s.W - r) % s.W) * gn) / s.W;

@@ -71,8 +71,15 @@ def test_schedule_properties(W, M, N, BM, BN, G, RG, order):
         # ranks run side by side
         assert np.array_equal(sched[:, 0], np.tile(np.arange(W), nM * nN))
     else:
-        # one rank after another, each rank's own order unchanged
-        assert np.array_equal(sched[:, 0], np.repeat(np.arange(W), nM * nN))
+        # per column group, one rank after another; each rank's own order unchanged
+        group = nN if G <= 0 or G >= nN else G
+        start = 0
+        for g0 in range(0, nN, group):
+            gn = min(group, nN - g0)
+            block = sched[start:start + W * nM * gn]
+            assert np.array_equal(block[:, 0], np.repeat(np.arange(W), nM * gn))
+            assert set(block[:, 2].tolist()) == set(range(g0, g0 + gn))
+            start += W * nM * gn
         side = oracle.schedule(W, M, N, BM, BN, G, RG, "interleaved")
         for r in range(W):
             assert np.array_equal(sched[sched[:, 0] == r], side[side[:, 0] == r])
@@ -155,20 +162,23 @@ def test_tile_contributions_arrive_in_step_order(W, M, N, BM, BN, G):
     (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
     (8, 4096, 4096, 256, 256, 8), (3, 300, 520, 128, 128, 0), (5, 5 * 256, 1000, 128, 256, 2)])
 def test_sequential_ranks_arrive_in_rank_order(W, M, N, BM, BN, G):
-    """With the ranks one after another, every output tile sees its W rank
-    contributions in rank order 0 .. W-1 (the order the chain reduction folds
-    in, the same as the last arriver's).  Rank r+1 reaches a tile at most one
-    of its steps (T/W entries) earlier in its own pass than rank r, give or take
-    the column offset, so consecutive contributions lie at least T*(W-2)/W
-    entries apart (T = tiles per rank)."""
+    """With the ranks one after another (per column group), every output tile
+    sees its W rank contributions in rank order 0 .. W-1 (the order the chain
+    reduction folds in, the same as the last arriver's).  Rank r+1 reaches a
+    tile at most one of its steps (T/W entries) earlier in its own pass over
+    the group than rank r, give or take the column offset, so consecutive
+    contributions lie at least T*(W-2)/W entries apart (T = a rank's tiles in
+    the tile's column group)."""
     sched = oracle.schedule(W, M, N, BM, BN, G, 0, "sequential")
     nM, nN = -(-M // BM), -(-N // BN)
-    T = nM * nN
+    group = nN if G <= 0 or G >= nN else G
     seen = {}
     for g, (r, mt, nt) in enumerate(sched.tolist()):
         seen.setdefault((mt, nt), []).append((g, r))
-    for lst in seen.values():
+    for (mt, nt), lst in seen.items():
         assert [r for _, r in lst] == list(range(W))
+        g0 = (nt // group) * group
+        T = nM * min(group, nN - g0)
         gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
         assert min(gaps) >= T * (W - 2) // W
 
