@@ -608,14 +608,26 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
+        // A quarter wholly below M (a short last row tile) has nothing to do.
+        const bool q_live = static_cast<int64_t>(mt) * kBM + q * 32 < a.M;
         float *tb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                     static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
         float *slot = tb + static_cast<int64_t>(sidx) * Cfg::kSlotFloats;
         const float *prev = tb; // slot 0: the running sum
+        if (!q_live) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (PAIR)
+                    ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->acc_empty[buf]), 0));
+                else
+                    ptx::mbar_arrive(ptx::smem_u32(&ctl->acc_empty[buf]));
+            }
+        }
         // The running sum is loaded before the slab's TMEM read; the other
         // warp of the lane quarter covers its latency.
 #pragma unroll 1
-        for (int slab = sl0; slab < sl1; ++slab) {
+        for (int slab = sl0; slab < (q_live ? sl1 : sl0); ++slab) {
             float4 rs[8];
             if (add_prev) {
 #pragma unroll
@@ -720,7 +732,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     // (no memset), and the tile goes to the reducers.
                     ptx::st_relaxed_gpu(flag, 0u);
                     for (int qq = 0; qq < 4 && ok; ++qq)
-                        ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
+                        if (static_cast<int64_t>(mt) * kBM + qq * 32 < a.M)
+                            ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
                 }
             } else {
                 int fold_from = -1;
@@ -755,7 +768,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 }
                 ptx::named_bar_sync(kBarEpi, nthr);
                 const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
-                fold_quarter<BN>(a, tile, q, lane, k, j, j == a.W - 1, sl0, sl1);
+                if (q_live)
+                    fold_quarter<BN>(a, tile, q, lane, k, j, j == a.W - 1, sl0, sl1);
                 ptx::named_bar_sync(kBarEpi, nthr);
                 if (etid == 0) {
                     int next = -1;
