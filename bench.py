@@ -306,6 +306,41 @@ def l2_note(w) -> str:
             "ms_per_step is the mean of the per-call CUDA-event times")
 
 
+def chunked_baseline(W, M, N, alpha, beta, y_code, Ad, Bd, Cd, Y, stream, dev):
+    """The chunked two-stream baseline (async-TP style, an unfused comparator):
+    for each output chunk c, the W per-rank GEMMs of the chunk's rows run on
+    `stream` into fp32 partials while the reduce of chunk c-1 runs on a second
+    stream; two chunk buffers alternate.  Returns a callable that runs one
+    call; `stream` has waited for all of its work when it returns."""
+    import torch
+    from tensor_gemm_reduce_tcgen05_gb300 import binding
+    R = M // W
+    s_red = torch.cuda.Stream(device=dev)
+    Pc = [torch.empty((W, R, N), dtype=torch.float32, device=dev) for _ in range(2)]
+    ev_p = [torch.cuda.Event() for _ in range(2)]
+    ev_r = [torch.cuda.Event() for _ in range(2)]
+    y_elt = Y.element_size()
+
+    def run():
+        for c in range(W):
+            buf = c % 2
+            if c >= 2:
+                stream.wait_event(ev_r[buf])  # chunk c-2's reduce is done with the buffer
+            with torch.cuda.stream(stream):
+                torch.bmm(Ad[:, c * R:(c + 1) * R, :], Bd, out_dtype=torch.float32, out=Pc[buf])
+            ev_p[buf].record(stream)
+            s_red.wait_event(ev_p[buf])
+            binding.gemm_rs_reduce_partials(
+                Pc[buf].data_ptr(), binding.GEMM_RS_FP32,
+                0 if Cd is None else Cd.data_ptr() + c * R * N * 2,
+                Y.data_ptr() + c * R * N * y_elt, R, N, W, alpha, beta, y_code,
+                s_red.cuda_stream)
+            ev_r[buf].record(s_red)
+        stream.wait_stream(s_red)
+
+    return run
+
+
 # --------------------------------------------------------------------------- our arm
 def time_loop(fn, steps, stream):
     import torch
@@ -460,6 +495,15 @@ def run_ours(args):
     reduce_ms = time_loop(reduce_only, args.steps, stream)
     del P
 
+    # chunked two-stream baseline (async-TP style)
+    chunked = chunked_baseline(w.W, w.M, w.N, w.alpha, w.beta, y_code, Ad, Bd, Cd, Y, stream, dev)
+    chunked_ms = None
+    if p_dtype == binding.GEMM_RS_FP32:
+        for _ in range(max(3, args.warmup)):
+            chunked()
+        chunked_ms = time_loop(chunked, args.steps, stream)
+    del chunked
+
     # full-K GEMM of the same shape (no reduce-scatter at all): context
     A_full = Ad.permute(1, 0, 2).reshape(w.M, w.K).contiguous()
     B_full = Bd.reshape(w.K, w.N)
@@ -557,6 +601,11 @@ def run_ours(args):
                         "value": w.flops / (unfused_ms / 1e3) / 1e12,
                         "gemms_ms": gemms_ms, "reduce_ms": reduce_ms, "partials": partials_note,
                         "fused_speedup": unfused_ms / ms_step},
+            "unfused_chunked": None if chunked_ms is None else {
+                "ms_per_step": chunked_ms, "value": w.flops / (chunked_ms / 1e3) / 1e12,
+                "chunks": w.W, "fused_speedup": chunked_ms / ms_step,
+                "note": "per chunk: W per-rank bmm (fp32 out) on one stream, reduce of the "
+                        "previous chunk on a second stream, two chunk buffers"},
             "full_k_gemm": {"ms": fullk_ms, "value": w.flops / (fullk_ms / 1e3) / 1e12,
                             "note": "torch.mm [M,K]x[K,N], no reduce-scatter (context)"},
             "kernel_ms_median": kernel_median_ms, "kernel_ms_min": kernel_min_ms,

@@ -263,3 +263,25 @@ def test_full_size_workloads_on_row_sample(name, mode, order):
     ref = oracle_y(A, B, C, w.alpha, w.beta, w.y_dtype, rows=rows)
     assert_close(y[rows], ref, w.y_dtype, name)
     assert int(op.flags_view().abs().sum()) == 0
+
+
+def test_chunked_two_stream_baseline_matches_oracle():
+    """The benchmark's chunked two-stream comparator (per-chunk cuBLAS GEMMs on
+    one stream, the reduce of the previous chunk on another) computes the same
+    Y: exact for integer-valued inputs."""
+    import bench
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 4, 512, 264, 64
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
+    dev = torch.device("cuda", 0)
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    for y_dtype in ("fp32", "bf16"):
+        Y = torch.empty((M, N), dtype=torch.float32 if y_dtype == "fp32" else torch.bfloat16,
+                        device=dev)
+        y_code = b.GEMM_RS_FP32 if y_dtype == "fp32" else b.GEMM_RS_BF16
+        run = bench.chunked_baseline(W, M, N, 0.5, 1.0, y_code, Ad, Bd, Cd, Y, stream, dev)
+        run()
+        run()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, C, 0.5, 1.0, y_dtype))
