@@ -338,6 +338,27 @@ struct gemm_rs_s {
 
 namespace {
 
+// Launch with programmatic stream serialization: the kernel's CTAs may start
+// (and set up shared memory and TMEM) while the previous kernel on the stream
+// finishes; each kernel waits (griddepcontrol.wait) before it touches global
+// memory.  With a non-kernel predecessor the launch is ordered as usual.
+template <typename Kern>
+cudaError_t launch_overlapped(Kern kernel, int grid, int smem, cudaStream_t s, const CUtensorMap &tmA,
+                              const CUtensorMap &tmB, const gemm_rs::KernelArgs &a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, a);
+}
+
 // Workers of the launch: CTA pairs for the 256-row tile, CTAs otherwise.
 int64_t workers_of(const gemm_rs_s *h)
 {
@@ -623,9 +644,8 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     if (h->bm == 2 * gemm_rs::kBM) {
         const int64_t pairs = h->pair_clusters;
         const int grid = static_cast<int>(2 * (a.total < pairs ? a.total : pairs));
-        gemm_rs::gemm_rs_pair_kernel<256>
-            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes_pair<256>(), s>>>(h->tmA, h->tmB, a);
-        e = cudaGetLastError();
+        e = launch_overlapped(gemm_rs::gemm_rs_pair_kernel<256>, grid,
+                              gemm_rs::smem_bytes_pair<256>(), s, h->tmA, h->tmB, a);
         if (e != cudaSuccess)
             return cuda_fail(e, "launch of the fused GEMM+RS pair kernel");
         return GEMM_RS_OK;
@@ -633,19 +653,18 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     const int grid = static_cast<int>(a.total < h->sms ? a.total : h->sms);
     switch (h->bn) {
     case 256:
-        gemm_rs::gemm_rs_fused_kernel<256>
-            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<256>(), s>>>(h->tmA, h->tmB, a);
+        e = launch_overlapped(gemm_rs::gemm_rs_fused_kernel<256>, grid, gemm_rs::smem_bytes<256>(), s,
+                              h->tmA, h->tmB, a);
         break;
     case 128:
-        gemm_rs::gemm_rs_fused_kernel<128>
-            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<128>(), s>>>(h->tmA, h->tmB, a);
+        e = launch_overlapped(gemm_rs::gemm_rs_fused_kernel<128>, grid, gemm_rs::smem_bytes<128>(), s,
+                              h->tmA, h->tmB, a);
         break;
     default:
-        gemm_rs::gemm_rs_fused_kernel<64>
-            <<<grid, gemm_rs::kThreads, gemm_rs::smem_bytes<64>(), s>>>(h->tmA, h->tmB, a);
+        e = launch_overlapped(gemm_rs::gemm_rs_fused_kernel<64>, grid, gemm_rs::smem_bytes<64>(), s,
+                              h->tmA, h->tmB, a);
         break;
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused GEMM+RS kernel");
     return GEMM_RS_OK;

@@ -375,15 +375,28 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             y[j] = ptx::ld_cg_f4(sb + j * 128);
+        // Two slots per round trip (16 loads in flight), added in slot order.
 #pragma unroll 1
-        for (int sl = first; sl <= hi; ++sl) {
-            float4 u[8];
+        for (int sl = first; sl <= hi; sl += 2) {
+            const bool two = sl + 1 <= hi;
+            float4 u[8], w2[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 u[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(sl) * Cfg::kSlotFloats + j * 128);
+            if (two) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    w2[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(sl + 1) * Cfg::kSlotFloats + j * 128);
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 y[j].x += u[j].x; y[j].y += u[j].y; y[j].z += u[j].z; y[j].w += u[j].w;
+            }
+            if (two) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    y[j].x += w2[j].x; y[j].y += w2[j].y; y[j].z += w2[j].z; y[j].w += w2[j].w;
+                }
             }
         }
         if (to_y) {
@@ -768,8 +781,17 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 }
                 ptx::named_bar_sync(kBarEpi, nthr);
                 const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
-                if (q_live)
-                    fold_quarter<BN>(a, tile, q, lane, k, j, j == a.W - 1, sl0, sl1);
+                // A fold reads only global memory, so the (quarter, slab) units
+                // of the live quarters are spread over all epilogue warps.
+                {
+                    const int64_t rows_left = a.M - static_cast<int64_t>(mt) * kBM;
+                    const int nlive = rows_left >= kBM ? 4 : static_cast<int>((rows_left + 31) / 32);
+                    const int units = nlive * Cfg::kSlabs;
+                    const int nw = nthr / 32;
+                    for (int u = (warp - kEpiWarp0); u < units; u += nw)
+                        fold_quarter<BN>(a, tile, u / Cfg::kSlabs, lane, k, j, j == a.W - 1,
+                                         u % Cfg::kSlabs, u % Cfg::kSlabs + 1);
+                }
                 ptx::named_bar_sync(kBarEpi, nthr);
                 if (etid == 0) {
                     int next = -1;
@@ -843,6 +865,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const Sched sch{a.W, a.nMs, a.nN, 7, a.R, a.colgroup, a.rowgroup, a.seq};
+    // Everything above touches only this CTA's shared memory and TMEM, so it
+    // may overlap the previous kernel on the stream; global memory waits.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0)
@@ -1070,6 +1096,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const Sched sch{a.W, a.nMs, a.nN, 8, a.R, a.colgroup, a.rowgroup, a.seq};
+    // Everything above touches only this CTA pair's shared memory and TMEM, so
+    // it may overlap the previous kernel on the stream; global memory waits.
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0)

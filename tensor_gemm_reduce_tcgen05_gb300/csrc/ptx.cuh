@@ -77,6 +77,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
 }
 
 // ---------------------------------------------------------------- TMA
+// Programmatic dependent launch.  wait: block until the grids this one
+// depends on (the previous kernel on the stream, when launched with
+// programmatic stream serialization) have completed and their memory
+// operations are visible; a no-op for a normal launch.  launch_dependents:
+// allow the next such kernel on the stream to start its CTAs as SMs free up.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
