@@ -626,6 +626,9 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.rowgroup = rowgroup_of(h);
     a.chain = h->reduce_mode == GEMM_RS_REDUCE_CHAIN ? 1 : 0;
     a.seq = sequential(h) ? 1 : 0;
+    // Sequential ranks reach a tile a rank's pass apart, and a single row tile
+    // brings all positions at once: neither gains from waiting for a turn.
+    a.chain_wait = (!a.seq && a.nMs > 1) ? 16384 : 0;
     a.R = h->M / h->W;
     a.total = static_cast<int64_t>(h->W) * a.nMs * a.nN;
     a.alpha = h->alpha;
@@ -892,6 +895,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.rowgroup = a.nM;
     a.chain = 1;
     a.seq = 1;
+    a.chain_wait = 0;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

@@ -112,6 +112,7 @@ struct KernelArgs {
     int rowgroup;   // row tiles per sweep (>= a chunk's row tiles: one sweep per step)
     int chain;      // 1: chain reduction (in-order fold as tiles land), 0: last arriver reduces
     int seq;        // 1: the ranks' tiles one rank after another, 0: the ranks side by side
+    long long chain_wait; // SM cycles a chain position waits for its turn before storing
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -437,7 +438,6 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
 // to slot 0 all happen before position i+1's, so every element is summed in
 // position order, the same order on every run.
 constexpr uint32_t kChainOwn = 1u << 24;
-constexpr long long kChainWaitCycles = 16384; // how long a position waits for its turn
 __device__ __forceinline__ uint32_t chain_k(uint32_t s) { return (s >> 16) & 31u; }
 
 // Take the fold at position i: true if positions 0 .. i-1 are folded, nobody
@@ -588,12 +588,14 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
                                  : ptx::mbar_wait(fb, aph, a.timeout, abort_flag);
         // If position pos-1 was not folded yet at the start, wait a little for
-        // it now that the accumulator has landed: a store and a later fold
-        // cost far more.  Late positions come mostly from the first step of a
-        // column group, whose B panels are not in L2 yet.
+        // it now that the accumulator has landed (a.chain_wait cycles; the host
+        // sets it where positions arrive staggered, as at the first step of a
+        // column group with the ranks side by side, whose B panels are not in
+        // L2 yet).  Where positions land together, storing at once and folding
+        // once is cheaper than a queue of waits.
         if (etid == 0 && a.chain && waited && half_ok && ctl->epi_direct[buf] == 0)
             ctl->epi_direct[buf] =
-                chain_wait_own(a.flags + tile, static_cast<uint32_t>(pos), kChainWaitCycles) ? 1 : 0;
+                chain_wait_own(a.flags + tile, static_cast<uint32_t>(pos), a.chain_wait) ? 1 : 0;
         if (ptx::named_bar_or(kBarEpi, nthr, !(waited && ok))) {
             ok = false;
             break;
