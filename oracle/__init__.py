@@ -5,7 +5,8 @@ benchmark's CPU-baseline leg may import this package.  The product path
 (the CUDA library and its Python binding) never does.  The oracle shares no
 code with the product path.
 
-The arithmetic lives in ``gemm_rs_oracle.c`` (plain C, fp64 accumulation).
+The arithmetic lives in ``gemm_rs_oracle.c`` (GEMM+RS) and ``ag_gemm_oracle.c``
+(AG+GEMM), plain C with fp64 accumulation.
 This module compiles it on first use and marshals numpy arrays into it.  The
 oracle's header comment states what is computed and which passages of the
 pages each step follows.
@@ -20,7 +21,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gemm_rs_oracle.c")
+_SRCS = [os.path.join(_HERE, "gemm_rs_oracle.c"), os.path.join(_HERE, "ag_gemm_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -29,11 +30,11 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the C oracle into ``oracle/liboracle.so`` and return its path."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
-           "-shared", "-fPIC", "-std=c11", "-Wall", "-o", tmp, _SRC]
+           "-shared", "-fPIC", "-std=c11", "-Wall", "-o", tmp] + _SRCS
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -52,6 +53,10 @@ def _load():
                                        i32, vp, i64, vp, vp, i32]
         lib.oracle_schedule.restype = i64
         lib.oracle_schedule.argtypes = [i32, i64, i64, i32, i32, i32, i32, i32, vp, i64]
+        lib.oracle_ag_gemm.restype = i32
+        lib.oracle_ag_gemm.argtypes = [i32, i64, i64, i64, f32, vp, vp, i32, vp, i64, vp, vp]
+        lib.oracle_ag_schedule.restype = i64
+        lib.oracle_ag_schedule.argtypes = [i32, i64, i64, i32, i32, vp, i64]
         lib.oracle_row_chunk.restype = i32
         lib.oracle_row_chunk.argtypes = [i32, i64, vp, vp]
         lib.oracle_bf16_from_float.restype = None
@@ -142,3 +147,38 @@ def float_from_bf16(x: np.ndarray) -> np.ndarray:
     out = np.empty(x.shape, dtype=np.float32)
     _load().oracle_float_from_bf16(x.ctypes.data, out.ctypes.data, x.size)
     return out
+
+
+def ag_gemm(X_bits: np.ndarray, B1_bits: np.ndarray, alpha: float, y_dtype: str,
+            rows=None, threads=None) -> np.ndarray:
+    """H[r] = alpha * X @ B1[r] for every rank r: X is [M][K] and B1 [W][K][N] as
+    bf16 bit patterns (uint16).  Returns [W][M][N] (or [W][len(rows)][N]) as
+    float32, or as uint16 bf16 bits when y_dtype == "bf16"."""
+    X_bits = np.ascontiguousarray(X_bits, dtype=np.uint16)
+    B1_bits = np.ascontiguousarray(B1_bits, dtype=np.uint16)
+    M, K = X_bits.shape
+    W, K2, N = B1_bits.shape
+    if K2 != K:
+        raise ValueError("X and B1 disagree on K")
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n_rows = M if rows_arr is None else rows_arr.shape[0]
+    y_bf16 = 1 if y_dtype == "bf16" else 0
+    out = np.zeros((W, n_rows, N), dtype=np.uint16 if y_bf16 else np.float32)
+    rc = _load().oracle_ag_gemm(W, M, N, K, ctypes.c_float(alpha), X_bits.ctypes.data,
+                                B1_bits.ctypes.data, y_bf16,
+                                None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+                                None if y_bf16 else out.ctypes.data,
+                                out.ctypes.data if y_bf16 else None)
+    if rc != 0:
+        raise ValueError(f"oracle_ag_gemm rejected its arguments (rc={rc})")
+    return out
+
+
+def ag_schedule(W: int, M: int, N: int, BM: int, BN: int) -> np.ndarray:
+    """AG+GEMM tile order as an int32 [W*T, 3] array of (r, mt, nt)."""
+    nM, nN = M // BM, -(-N // BN)
+    out = np.zeros((W * nM * nN, 3), dtype=np.int32)
+    n = _load().oracle_ag_schedule(W, M, N, BM, BN, out.ctypes.data, out.shape[0])
+    if n < 0:
+        raise ValueError(f"oracle_ag_schedule rejected its arguments (rc={n})")
+    return out[:n]
