@@ -623,6 +623,144 @@ def run_ours(args):
     return 0
 
 
+AG_METRIC = "fused AG+GEMM TFLOP/s and % of GB300 bf16 tensor peak vs unfused, 1 GPU"
+
+
+def run_ag(args):
+    """The AG+GEMM half of the FFN (the first GEMM, all-gathered rows): one JSON
+    line with the fused kernel's throughput, the unfused same-GPU baseline
+    (the all-gather as W*(W-1) chunk copies into per-rank buffers, then one
+    batched cuBLAS GEMM) and a plain batched GEMM without any gather."""
+    import torch
+    from tensor_gemm_reduce_tcgen05_gb300 import binding
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import AG_WORKLOADS, bf16_bits, make_ag_inputs
+
+    w = AG_WORKLOADS[args.workload if args.workload in AG_WORKLOADS else "ag_ffn_w8_m4096"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+    X, B1 = make_ag_inputs(w.W, w.M, w.N, w.K, w.x_dist, w.b_dist)
+    Xd, Bd = X.to(dev), B1.to(dev)
+    op = binding.AgGemm(w.M, w.N, w.K, w.W, w.alpha, w.y_dtype, device=dev)
+    H = op.new_output()
+
+    def step():
+        op.run(Xd, Bd, H, stream)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout during warm-up: " + binding.gemm_rs_last_error())
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+    ms_step = t0.elapsed_time(t1) / args.steps
+    kernel_ms = sorted(a.elapsed_time(b) for a, b in zip(starts, ends))
+    kernel_avg = sum(kernel_ms) / len(kernel_ms)
+    value = w.flops / (ms_step / 1e3) / 1e12
+
+    # unfused: the all-gather as chunk copies into per-rank buffers, then bmm
+    R = w.M // w.W
+    G = torch.empty((w.W, w.M, w.K), dtype=torch.bfloat16, device=dev)
+    Hu = torch.empty((w.W, w.M, w.N), dtype=torch.bfloat16 if w.y_dtype == "bf16" else torch.float32,
+                     device=dev)
+
+    def gemm():
+        torch.bmm(G, Bd, out=Hu) if Hu.dtype == torch.bfloat16 else \
+            torch.bmm(G, Bd, out_dtype=torch.float32, out=Hu)
+
+    def gather():
+        G.copy_(Xd.unsqueeze(0).expand(w.W, w.M, w.K))  # one copy kernel for all ranks
+
+    def gather_chunks():
+        for r in range(w.W):
+            for c in range(w.W):
+                if c != r:
+                    G[r, c * R:(c + 1) * R].copy_(Xd[c * R:(c + 1) * R])
+
+    def unfused():
+        gather()
+        gemm()
+
+    def unfused_chunks():
+        gather_chunks()
+        gemm()
+
+    def plain():
+        torch.matmul(Xd, Bd, out=Hu)
+
+    for _ in range(3):
+        unfused()
+        unfused_chunks()
+        plain()
+    unfused_ms = time_loop(unfused, args.steps, stream)
+    gather_ms = time_loop(gather, args.steps, stream)
+    chunks_ms = time_loop(unfused_chunks, args.steps, stream)
+    plain_ms = time_loop(plain, args.steps, stream)
+    clocks = sampler.stop()
+    del G, Hu
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        cores = host_cores()
+        rows = np.linspace(0, w.M - 1, 8).astype(np.int64)
+        t = time.perf_counter()
+        oracle.ag_gemm(bf16_bits(X), bf16_bits(B1), w.alpha, w.y_dtype, rows=rows, threads=cores)
+        sec = time.perf_counter() - t
+        cpu = {"value": 2.0 * len(rows) * w.W * w.N * w.K / sec / 1e12, "unit": "TFLOP/s",
+               "cores": cores, "kind": "oracle", "seconds": sec,
+               "sample": f"{len(rows)} of {w.M} rows of every rank's output, evenly spaced"}
+
+    achieved = w.flops / (kernel_avg / 1e3) / 1e12
+    line = {
+        "metric": AG_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "W": w.W, "M": w.M, "N_per_rank": w.N, "K": w.K,
+                   "alpha": w.alpha, "y_dtype": w.y_dtype,
+                   "inputs": f"X {w.x_dist}, B1 {w.b_dist}",
+                   "l2": "inputs larger than L2: gather buffers "
+                         f"{w.W * w.M * w.K * 2 / 1e6:.0f} MB, no flush between steps"},
+        "pct_of_peak": 100.0 * achieved / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                     "kernel": "ag_gemm_pair_kernel", "kernel_ms": kernel_avg, "traffic": None},
+        "kernel_ms_median": kernel_ms[len(kernel_ms) // 2], "kernel_ms_min": kernel_ms[0],
+        "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": cpu,
+        "unfused": {"ms_per_step": unfused_ms, "value": w.flops / (unfused_ms / 1e3) / 1e12,
+                    "gather_ms": gather_ms, "fused_speedup": unfused_ms / ms_step,
+                    "note": "the all-gather as one copy of X into every rank's buffer, then "
+                            "torch.bmm"},
+        "unfused_chunk_copies": {"ms_per_step": chunks_ms,
+                                 "value": w.flops / (chunks_ms / 1e3) / 1e12,
+                                 "note": "W*(W-1) chunk copies (one per rank and remote chunk), "
+                                         "then torch.bmm"},
+        "plain_gemm": {"ms": plain_ms, "value": w.flops / (plain_ms / 1e3) / 1e12,
+                       "note": "torch.matmul X [M,K] x B1 [W,K,N], no gather (context)"},
+        "plan": op.plan,
+    }
+    print(json.dumps(line))
+    op.close()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,6 +768,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_w8_m4096")
+    ap.add_argument("--path", choices=["gemm_rs", "ag"], default="gemm_rs",
+                    help="gemm_rs: the fused GEMM + reduce-scatter (the default line); "
+                         "ag: the fused all-gather + GEMM")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -642,6 +783,8 @@ def main(argv=None):
     args.steps = max(1, args.steps)
     if args.impl == "reference":
         return run_reference(args)
+    if args.path == "ag":
+        return run_ag(args)
     return run_ours(args)
 
 

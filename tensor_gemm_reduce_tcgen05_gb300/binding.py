@@ -1,4 +1,4 @@
-"""ctypes binding of the C ABI in ``include/gemm_rs.h``.
+"""ctypes binding of the C ABI in ``include/gemm_rs.h`` and ``include/ag_gemm.h``.
 
 Each function has the C function's name and only marshals arguments.  Device
 pointers and streams are passed as Python ints (``tensor.data_ptr()``,
@@ -6,7 +6,7 @@ pointers and streams are passed as Python ints (``tensor.data_ptr()``,
 CUDA library.  If the library is missing, :func:`lib` raises instead of
 falling back to anything else.
 
-:class:`GemmRS` is a convenience owner for a handle.  It keeps a torch-allocated
+:class:`GemmRS` and :class:`AgGemm` are convenience owners of a handle.  It keeps a torch-allocated
 workspace and accepts torch tensors.  PyTorch is used there only for device
 memory and the current stream.
 """
@@ -40,6 +40,8 @@ GEMM_RS_REDUCE_LAST_ARRIVER = 1
 GEMM_RS_RANKS_DEFAULT = 0
 GEMM_RS_RANKS_SEQUENTIAL = 1
 GEMM_RS_RANKS_INTERLEAVED = 2
+
+AG_GEMM_DEBUG_SKIP_COPIES = 1
 
 _DTYPES = {"bf16": GEMM_RS_BF16, "fp32": GEMM_RS_FP32}
 
@@ -87,6 +89,16 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_reduce_partials": (i32, [vp, i32, vp, vp, i64, i64, i32, f32, f32, i32, vp]),
             "gemm_rs_version": (ctypes.c_char_p, []),
             "gemm_rs_run_noalloc": (i32, [i64, i64, i64, i32, f32, f32, i32, vp, vp, vp, vp, vp]),
+            "ag_gemm_workspace_bytes": (sz, [i64, i64, i64, i32]),
+            "ag_gemm_create": (i32, [ctypes.POINTER(vp), i64, i64, i64, i32, f32, i32, vp, sz, vp]),
+            "ag_gemm_run": (i32, [vp, vp, vp, vp, vp]),
+            "ag_gemm_status": (i32, [vp, vp]),
+            "ag_gemm_reset": (i32, [vp, vp]),
+            "ag_gemm_destroy": (i32, [vp]),
+            "ag_gemm_schedule": (i64, [i64, i64, i32, vp, i64]),
+            "ag_gemm_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 4),
+            "ag_gemm_set_timeout_cycles": (i32, [vp, u64]),
+            "ag_gemm_set_debug": (i32, [vp, vp, i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -278,6 +290,130 @@ class GemmRS:
     def close(self) -> None:
         if getattr(self, "handle", None) is not None:
             gemm_rs_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# --------------------------------------------------------------------------- AG+GEMM
+def ag_gemm_workspace_bytes(M: int, N: int, K: int, W: int) -> int:
+    return lib().ag_gemm_workspace_bytes(M, N, K, W)
+
+
+def ag_gemm_create(M, N, K, W, alpha, y_dtype, workspace, workspace_bytes, stream=0):
+    h = ctypes.c_void_p()
+    _check(lib().ag_gemm_create(ctypes.byref(h), M, N, K, W, alpha, y_dtype, workspace,
+                                workspace_bytes, stream))
+    return h
+
+
+def ag_gemm_run(h, X, B1, H, stream=0) -> None:
+    _check(lib().ag_gemm_run(h, X, B1, H, stream))
+
+
+def ag_gemm_status(h, stream=0) -> int:
+    rc = lib().ag_gemm_status(h, stream)
+    if rc not in (GEMM_RS_OK, GEMM_RS_ERR_TIMEOUT):
+        _check(rc)
+    return rc
+
+
+def ag_gemm_reset(h, stream=0) -> None:
+    _check(lib().ag_gemm_reset(h, stream))
+
+
+def ag_gemm_destroy(h) -> None:
+    _check(lib().ag_gemm_destroy(h))
+
+
+def ag_gemm_schedule(M: int, N: int, W: int) -> np.ndarray:
+    nM, nN = M // 256, -(-N // 256)
+    out = np.zeros((W * nM * nN, 3), dtype=np.int32)
+    n = _check(lib().ag_gemm_schedule(M, N, W, out.ctypes.data, out.shape[0]))
+    return out[:n]
+
+
+def ag_gemm_get_plan(h) -> dict:
+    v = [ctypes.c_int() for _ in range(4)]
+    _check(lib().ag_gemm_get_plan(h, *[ctypes.byref(x) for x in v]))
+    return dict(zip(("grid", "stages", "slice_rows", "slices"), (x.value for x in v)))
+
+
+def ag_gemm_set_timeout_cycles(h, cycles: int) -> None:
+    _check(lib().ag_gemm_set_timeout_cycles(h, cycles))
+
+
+def ag_gemm_set_debug(h, record_ptr: int = 0, flags: int = 0) -> None:
+    _check(lib().ag_gemm_set_debug(h, record_ptr, flags))
+
+
+class AgGemm:
+    """Owns one AG+GEMM handle and its workspace (a torch uint8 CUDA tensor).
+
+    H[r] = alpha * X @ B1[r] for r = 0 .. W-1, where X ([M, K] bf16) is the
+    all-gather of W row chunks and B1 ([W, K, N] bf16) holds the ranks' column
+    shards.  H is [W, M, N] in y_dtype.
+    """
+
+    def __init__(self, M: int, N: int, K: int, W: int, alpha: float = 1.0, y_dtype: str = "bf16",
+                 device=None, stream=None):
+        import torch
+        lib()
+        self.M, self.N, self.K, self.W = M, N, K, W
+        self.alpha, self.y_dtype = alpha, y_dtype
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        nbytes = ag_gemm_workspace_bytes(M, N, K, W)
+        if nbytes == 0:
+            lib().ag_gemm_create(ctypes.byref(ctypes.c_void_p()), M, N, K, W, alpha, 0, None, 0, None)
+            _check(GEMM_RS_ERR_SHAPE)
+        with torch.cuda.device(self.device):
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            self.handle = ag_gemm_create(M, N, K, W, alpha, _DTYPES[y_dtype],
+                                         self.workspace.data_ptr(), nbytes, _stream_ptr(stream))
+
+    @property
+    def plan(self) -> dict:
+        return ag_gemm_get_plan(self.handle)
+
+    def new_output(self):
+        import torch
+        dt = torch.bfloat16 if self.y_dtype == "bf16" else torch.float32
+        return torch.empty((self.W, self.M, self.N), dtype=dt, device=self.device)
+
+    def run(self, X, B1, H=None, stream=None):
+        """Launch once (asynchronous).  Returns H."""
+        import torch
+        for t, name in ((X, "X"), (B1, "B1")):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"{name} must be a contiguous bf16 tensor on {self.device}")
+        if tuple(X.shape) != (self.M, self.K):
+            raise ValueError(f"X must be [M, K] = {(self.M, self.K)}")
+        if tuple(B1.shape) != (self.W, self.K, self.N):
+            raise ValueError(f"B1 must be [W, K, N] = {(self.W, self.K, self.N)}")
+        if H is None:
+            H = self.new_output()
+        ag_gemm_run(self.handle, X.data_ptr(), B1.data_ptr(), H.data_ptr(), _stream_ptr(stream))
+        return H
+
+    def status(self, stream=None) -> int:
+        return ag_gemm_status(self.handle, _stream_ptr(stream))
+
+    def reset(self, stream=None) -> None:
+        ag_gemm_reset(self.handle, _stream_ptr(stream))
+
+    def signals_view(self):
+        """The W*W chunk signals (a view into the workspace), for tests."""
+        import torch
+        return self.workspace[256:256 + 4 * self.W * self.W].view(torch.int32)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None:
+            ag_gemm_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

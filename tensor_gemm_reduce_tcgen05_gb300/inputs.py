@@ -99,6 +99,38 @@ def workload_inputs(w: Workload, exact: bool = False, seeds=(1, 2, 3)):
     return make_inputs(w.W, w.M, w.N, w.Kpr, w.a_dist, w.b_dist, w.c_dist, seeds)
 
 
+@dataclass(frozen=True)
+class AgWorkload:
+    """An AG+GEMM workload: H_r = alpha * X @ B1_r, X [M, K], B1 [W, K, N]."""
+    name: str
+    W: int
+    M: int
+    N: int  # columns per rank
+    K: int
+    x_dist: str
+    b_dist: str
+    alpha: float
+    y_dtype: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.W * self.M * self.N * self.K
+
+
+# The FFN's first GEMM in front of the 4096x4096 W=8 GEMM+RS workload: hidden
+# 4096, FFN width 14336 = 8 x 1792 (its output H_r is that workload's A_r).
+AG_WORKLOADS = {
+    "ag_ffn_w8_m4096": AgWorkload("ag_ffn_w8_m4096", 8, 4096, 1792, 4096, "normal", "normal",
+                                  1.0, "bf16"),
+}
+
+
+def make_ag_inputs(W: int, M: int, N: int, K: int, x_dist: str = "normal", b_dist: str = "normal",
+                   seeds=(11, 12)):
+    """CPU bf16 tensors X [M, K] and B1 [W, K, N]."""
+    return _draw((M, K), x_dist, seeds[0]), _draw((W, K, N), b_dist, seeds[1])
+
+
 def bf16_bits(t: torch.Tensor):
     """The raw bit patterns of a CPU bf16 tensor as a numpy uint16 array."""
     import numpy as np

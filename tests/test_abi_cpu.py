@@ -1,6 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol
-include/gemm_rs.h declares, validates arguments before touching the device,
-and its host-side tile schedule equals the oracle's bit for bit."""
+include/gemm_rs.h and include/ag_gemm.h declare, validates arguments before
+touching the device, and its host-side tile schedules equal the oracle's bit
+for bit."""
 import os
 import re
 
@@ -11,6 +12,7 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gemm_rs.h")
+HEADERS = [HEADER, os.path.join(ROOT, "include", "ag_gemm.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,21 +24,25 @@ def b():
 
 
 def _declared():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_rs_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:gemm_rs|ag_gemm)_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(b):
     names = _declared()
     assert "gemm_rs_create" in names and "gemm_rs_run" in names and "gemm_rs_destroy" in names
+    assert "ag_gemm_create" in names and "ag_gemm_run" in names and "ag_gemm_destroy" in names
     L = b.lib()
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
 
 
-def test_no_torch_types_in_header():
-    text = open(HEADER).read()
+@pytest.mark.parametrize("path", ["gemm_rs.h", "ag_gemm.h"])
+def test_no_torch_types_in_header(path):
+    text = open(os.path.join(ROOT, "include", path)).read()
     assert "torch" not in text.lower().replace("pytorch", "")
     assert "at::" not in text and "c10" not in text
 
@@ -126,3 +132,19 @@ def test_reduce_partials_validates(b):
     assert L.gemm_rs_reduce_partials(None, 1, None, None, 4, 16, 0, 1.0, 0.0, 1, None) == \
         b.GEMM_RS_ERR_ARG
     assert L.gemm_rs_reduce_partials(None, 1, None, None, 0, 16, 2, 1.0, 0.0, 1, None) == 0
+
+
+@pytest.mark.parametrize("W,M,N", [(1, 256, 72), (2, 512, 256), (8, 2048, 768), (8, 4096, 1792),
+                                   (3, 1536, 1000), (16, 16 * 256, 64)])
+def test_ag_schedule_matches_oracle(b, W, M, N):
+    np.testing.assert_array_equal(b.ag_gemm_schedule(M, N, W), oracle.ag_schedule(W, M, N, 256, 256))
+
+
+def test_ag_shape_checks(b):
+    assert b.ag_gemm_workspace_bytes(4096, 1792, 4096, 8) == 256 + 256 + 8 * 4096 * 4096 * 2
+    assert b.ag_gemm_workspace_bytes(4096 - 256, 1792, 4096, 8) == 0   # 256-row tiles straddle chunks
+    assert b.ag_gemm_workspace_bytes(4096, 1790, 4096, 8) == 0         # N not a multiple of 8
+    assert b.ag_gemm_workspace_bytes(4096, 1792, 4092, 8) == 0         # K not a multiple of 8
+    assert b.ag_gemm_workspace_bytes(4096, 1792, 4096, 17) == 0
+    with pytest.raises(b.GemmRSError):
+        b.ag_gemm_schedule(300, 256, 2)
