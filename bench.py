@@ -761,6 +761,91 @@ def run_ag(args):
     return 0
 
 
+FFN_METRIC = "fused TP FFN (AG+GEMM then GEMM+RS) TFLOP/s vs unfused, 1 GPU"
+
+
+def run_ffn(args):
+    """The tensor-parallel FFN chain: AG+GEMM (X -> H) then GEMM+RS (H -> Y), on
+    the shapes of the default GEMM+RS workload, through ffn_tp_run; against
+    the unfused chain and against the two fused kernels timed alone."""
+    import torch
+    from tensor_gemm_reduce_tcgen05_gb300 import binding
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import AG_WORKLOADS, WORKLOADS, make_ag_inputs
+
+    wa = AG_WORKLOADS["ag_ffn_w8_m4096"]
+    wr = WORKLOADS["ffn_w8_m4096"]
+    assert wr.W == wa.W and wr.M == wa.M and wr.Kpr == wa.N
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+    X, B1 = make_ag_inputs(wa.W, wa.M, wa.N, wa.K, wa.x_dist, wa.b_dist)
+    g = torch.Generator().manual_seed(2)
+    B2 = (torch.randn((wr.W, wr.Kpr, wr.N), generator=g) * 0.02).to(torch.bfloat16)
+    Xd, B1d, B2d = X.to(dev), B1.to(dev), B2.to(dev)
+    ag = binding.AgGemm(wa.M, wa.N, wa.K, wa.W, wa.alpha, "bf16", device=dev)
+    rs = binding.GemmRS(wr.M, wr.N, wr.K, wr.W, wr.alpha, wr.beta, wr.y_dtype, device=dev)
+    H = ag.new_output()
+    Y = rs.new_output()
+    flops = wa.flops + wr.flops
+
+    def chain():
+        binding.ffn_tp_run(ag.handle, rs.handle, Xd.data_ptr(), B1d.data_ptr(), H.data_ptr(),
+                           B2d.data_ptr(), 0, Y.data_ptr(), stream.cuda_stream)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    for _ in range(args.warmup):
+        chain()
+    torch.cuda.synchronize()
+    if ag.status(stream) != 0 or rs.status(stream) != 0:
+        raise RuntimeError("device timeout during warm-up: " + binding.gemm_rs_last_error())
+    ms_step = time_loop(chain, args.steps, stream)
+    ag_ms = time_loop(lambda: ag.run(Xd, B1d, H, stream), args.steps, stream)
+    rs_ms = time_loop(lambda: rs.run(H, B2d, None, Y, stream), args.steps, stream)
+    if ag.status(stream) != 0 or rs.status(stream) != 0:
+        raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+
+    # unfused chain: gather copy, bmm, bmm into fp32 partials, the reduce kernel
+    G = torch.empty((wa.W, wa.M, wa.K), dtype=torch.bfloat16, device=dev)
+    Hu = torch.empty((wa.W, wa.M, wa.N), dtype=torch.bfloat16, device=dev)
+    P = torch.empty((wr.W, wr.M, wr.N), dtype=torch.float32, device=dev)
+    y_code = binding.GEMM_RS_BF16 if wr.y_dtype == "bf16" else binding.GEMM_RS_FP32
+
+    def unfused():
+        G.copy_(Xd.unsqueeze(0).expand(wa.W, wa.M, wa.K))
+        torch.bmm(G, B1d, out=Hu)
+        torch.bmm(Hu, B2d, out_dtype=torch.float32, out=P)
+        binding.gemm_rs_reduce_partials(P.data_ptr(), binding.GEMM_RS_FP32, 0, Y.data_ptr(), wr.M,
+                                        wr.N, wr.W, wr.alpha, wr.beta, y_code, stream.cuda_stream)
+
+    for _ in range(3):
+        unfused()
+    unfused_ms = time_loop(unfused, args.steps, stream)
+    clocks = sampler.stop()
+    del G, Hu, P
+
+    line = {
+        "metric": FFN_METRIC, "value": flops / (ms_step / 1e3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "ffn_tp_w8_m4096", "W": wa.W, "M": wa.M, "hidden": wa.K,
+                   "ffn_per_rank": wa.N, "y_dtype": wr.y_dtype, "activation": "none",
+                   "l2": "inputs larger than L2, no flush between steps"},
+        "pct_of_peak": 100.0 * flops / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "stages": {"ag_gemm_ms": ag_ms, "gemm_rs_ms": rs_ms},
+        "unfused": {"ms_per_step": unfused_ms, "value": flops / (unfused_ms / 1e3) / 1e12,
+                    "fused_speedup": unfused_ms / ms_step,
+                    "note": "gather copy, bmm, bmm into fp32 partials, separate reduce kernel"},
+    }
+    print(json.dumps(line))
+    ag.close()
+    rs.close()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -768,9 +853,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_w8_m4096")
-    ap.add_argument("--path", choices=["gemm_rs", "ag"], default="gemm_rs",
+    ap.add_argument("--path", choices=["gemm_rs", "ag", "ffn"], default="gemm_rs",
                     help="gemm_rs: the fused GEMM + reduce-scatter (the default line); "
-                         "ag: the fused all-gather + GEMM")
+                         "ag: the fused all-gather + GEMM; ffn: both, chained")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -785,6 +870,8 @@ def main(argv=None):
         return run_reference(args)
     if args.path == "ag":
         return run_ag(args)
+    if args.path == "ffn":
+        return run_ffn(args)
     return run_ours(args)
 
 

@@ -107,6 +107,27 @@ enum {
  * (r, mt, nt, worker) per entry, or NULL) and set debug flags. */
 GEMM_RS_API int ag_gemm_set_debug(ag_gemm_t h, int32_t *record, int flags);
 
+/* The handle's shape and output dtype (host outputs; any pointer may be NULL). */
+GEMM_RS_API int ag_gemm_get_shape(ag_gemm_t h, int64_t *M, int64_t *N, int64_t *K, int *W,
+                                  int *y_dtype);
+
+/*
+ * The tensor-parallel FFN on one GPU, both halves fused with their collective
+ * ("通信 overlap 实现", the passage on why AG and RS cannot simply be issued
+ * asynchronously: the AG output is the GEMM input and the GEMM output is the
+ * RS input, so the chain is split into tile-level steps):
+ *
+ *     H_r = alpha1 * X @ B1_r                    (ag, bf16 output)
+ *     Y   = sum_r (alpha2 * H_r @ B2_r + beta * C)   (rs, chunk c = rows of chunk c)
+ *
+ * Two launches on `stream`: the AG+GEMM, then the GEMM+RS with A = H.  No
+ * activation is applied between them.  `ag` must have a bf16 output and `rs`
+ * the matching shape: same M and W, rs K = W * (ag N).  Pointers as in
+ * ag_gemm_run (X, B1, H) and gemm_rs_run (B2 = its B, C, Y).
+ */
+GEMM_RS_API int ffn_tp_run(ag_gemm_t ag, gemm_rs_t rs, const void *X, const void *B1, void *H,
+                           const void *B2, const void *C, void *Y, gemm_rs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

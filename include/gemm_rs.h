@@ -231,6 +231,10 @@ GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
                                  int *colgroup, int *rowgroup, int *rank_order, int *reduce_mode);
 
+/* The handle's shape and output dtype (host outputs; any pointer may be NULL). */
+GEMM_RS_API int gemm_rs_get_shape(gemm_rs_t h, int64_t *M, int64_t *N, int64_t *K, int *W,
+                                  int *y_dtype);
+
 /* Override the tile width (bn = 256, 128 or 64) of the single-CTA kernel
  * (bm = 128).  Returns ERR_ARG for any other value. */
 GEMM_RS_API int gemm_rs_set_tile_n(gemm_rs_t h, int bn);

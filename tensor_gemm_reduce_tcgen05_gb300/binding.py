@@ -99,6 +99,13 @@ def lib() -> ctypes.CDLL:
             "ag_gemm_get_plan": (i32, [vp] + [ctypes.POINTER(i32)] * 4),
             "ag_gemm_set_timeout_cycles": (i32, [vp, u64]),
             "ag_gemm_set_debug": (i32, [vp, vp, i32]),
+            "ag_gemm_get_shape": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                        ctypes.POINTER(i64), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]),
+            "gemm_rs_get_shape": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                        ctypes.POINTER(i64), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]),
+            "ffn_tp_run": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -421,3 +428,8 @@ class AgGemm:
             self.close()
         except Exception:
             pass
+
+
+def ffn_tp_run(ag_handle, rs_handle, X, B1, H, B2, C, Y, stream=0) -> None:
+    """AG+GEMM then GEMM+RS with A = H (device pointers as ints)."""
+    _check(lib().ffn_tp_run(ag_handle, rs_handle, X, B1, H, B2, C, Y, stream))

@@ -370,4 +370,43 @@ int ag_gemm_set_debug(ag_gemm_t h, int32_t *record, int flags)
     return GEMM_RS_OK;
 }
 
+int ag_gemm_get_shape(ag_gemm_t h, int64_t *M, int64_t *N, int64_t *K, int *W, int *y_dtype)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (M)
+        *M = h->M;
+    if (N)
+        *N = h->N;
+    if (K)
+        *K = h->K;
+    if (W)
+        *W = h->W;
+    if (y_dtype)
+        *y_dtype = h->y_dtype;
+    return GEMM_RS_OK;
+}
+
+int ffn_tp_run(ag_gemm_t ag, gemm_rs_t rs, const void *X, const void *B1, void *H, const void *B2,
+               const void *C, void *Y, gemm_rs_stream_t stream)
+{
+    if (ag == nullptr || rs == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "both handles are needed");
+    int64_t rM = 0, rK = 0;
+    int rW = 0;
+    int rc = gemm_rs_get_shape(rs, &rM, nullptr, &rK, &rW, nullptr);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    if (ag->y_dtype != GEMM_RS_BF16)
+        return fail(GEMM_RS_ERR_UNSUPPORTED, "the AG+GEMM output feeds the GEMM+RS: it must be bf16");
+    if (rM != ag->M || rW != ag->W || rK != static_cast<int64_t>(ag->W) * ag->N)
+        return fail(GEMM_RS_ERR_SHAPE,
+                    "GEMM+RS shape (M=%lld, K=%lld, W=%d) does not continue the AG+GEMM "
+                    "(M=%lld, N=%lld per rank, W=%d)",
+                    (long long)rM, (long long)rK, rW, (long long)ag->M, (long long)ag->N, ag->W);
+    if ((rc = ag_gemm_run(ag, X, B1, H, stream)) != GEMM_RS_OK)
+        return rc;
+    return gemm_rs_run(rs, H, B2, C, Y, stream);
+}
+
 } // extern "C"

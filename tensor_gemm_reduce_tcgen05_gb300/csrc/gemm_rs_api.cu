@@ -436,6 +436,23 @@ int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid, int 
     return GEMM_RS_OK;
 }
 
+int gemm_rs_get_shape(gemm_rs_t h, int64_t *M, int64_t *N, int64_t *K, int *W, int *y_dtype)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (M)
+        *M = h->M;
+    if (N)
+        *N = h->N;
+    if (K)
+        *K = h->K;
+    if (W)
+        *W = h->W;
+    if (y_dtype)
+        *y_dtype = h->y_dtype;
+    return GEMM_RS_OK;
+}
+
 int gemm_rs_set_tile_n(gemm_rs_t h, int bn)
 {
     if (h == nullptr)

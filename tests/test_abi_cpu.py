@@ -27,7 +27,7 @@ def _declared():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:gemm_rs|ag_gemm)_[a-z_]+)\s*\(", text))
+        names |= set(re.findall(r"\b((?:gemm_rs|ag_gemm|ffn_tp)_[a-z_]+)\s*\(", text))
     return sorted(names)
 
 
@@ -35,6 +35,7 @@ def test_exports_every_declared_symbol(b):
     names = _declared()
     assert "gemm_rs_create" in names and "gemm_rs_run" in names and "gemm_rs_destroy" in names
     assert "ag_gemm_create" in names and "ag_gemm_run" in names and "ag_gemm_destroy" in names
+    assert "ffn_tp_run" in names
     L = b.lib()
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
