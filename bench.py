@@ -105,10 +105,13 @@ def load_peaks():
 KERNEL_SOURCES = ("gemm_rs_kernel.cuh", "ptx.cuh", "schedule.cuh")
 
 
-def kernel_source_hash() -> str:
+AG_KERNEL_SOURCES = ("ag_gemm_kernel.cuh", "gemm_rs_kernel.cuh", "ptx.cuh")
+
+
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_gemm_reduce_tcgen05_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -116,6 +119,8 @@ def kernel_source_hash() -> str:
 
 
 def plan_key(plan) -> str:
+    if "slices" in plan:  # the AG+GEMM plan
+        return "grid={grid} stages={stages} slice_rows={slice_rows} slices={slices}".format(**plan)
     return ("bm={bm} bn={bn} colgroup={colgroup} rowgroup={rowgroup} rank_order={rank_order} "
             "reduce_mode={reduce_mode}").format(**plan)
 
@@ -125,7 +130,7 @@ def kernel_name(plan) -> str:
     return "gemm_rs_pair_kernel" if plan["bm"] == 256 else "gemm_rs_fused_kernel"
 
 
-def recorded_traffic(kernel: str, workload: str, plan):
+def recorded_traffic(kernel: str, workload: str, plan, sources=KERNEL_SOURCES):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary,
     if that summary was taken on the current kernel source and the same plan."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
@@ -135,7 +140,7 @@ def recorded_traffic(kernel: str, workload: str, plan):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]+)\s+plan:\s*([^\n]+)",
                   text)
-    if not m or m.group(2) != kernel_source_hash() or m.group(3).strip() != plan_key(plan):
+    if not m or m.group(2) != kernel_source_hash(sources) or m.group(3).strip() != plan_key(plan):
         return None
     return int(m.group(1))
 
@@ -672,6 +677,12 @@ def run_ag(args):
     kernel_ms = sorted(a.elapsed_time(b) for a, b in zip(starts, ends))
     kernel_avg = sum(kernel_ms) / len(kernel_ms)
     value = w.flops / (ms_step / 1e3) / 1e12
+    if args.skip_extras:
+        print(json.dumps({"metric": AG_METRIC, "value": value, "unit": "TFLOP/s",
+                          "ms_per_step": ms_step, "kernel_ms": kernel_avg, "plan": op.plan,
+                          "clocks": sampler.stop(), "note": "profiling run: fused kernel only"}))
+        op.close()
+        return 0
 
     # unfused: the all-gather as chunk copies into per-rank buffers, then bmm
     R = w.M // w.W
@@ -741,7 +752,9 @@ def run_ag(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-                     "kernel": "ag_gemm_pair_kernel", "kernel_ms": kernel_avg, "traffic": None},
+                     "kernel": "ag_gemm_pair_kernel", "kernel_ms": kernel_avg,
+                     "traffic": recorded_traffic("ag_gemm_pair_kernel", w.name, op.plan,
+                                                 AG_KERNEL_SOURCES)},
         "kernel_ms_median": kernel_ms[len(kernel_ms) // 2], "kernel_ms_min": kernel_ms[0],
         "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": cpu,
         "unfused": {"ms_per_step": unfused_ms, "value": w.flops / (unfused_ms / 1e3) / 1e12,
