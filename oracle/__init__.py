@@ -53,6 +53,9 @@ def _load():
                                        i32, vp, i64, vp, vp, i32]
         lib.oracle_schedule.restype = i64
         lib.oracle_schedule.argtypes = [i32, i64, i64, i32, i32, i32, i32, i32, vp, i64]
+        lib.oracle_gemm_rs_two_level.restype = i32
+        lib.oracle_gemm_rs_two_level.argtypes = [i32, i64, i64, i64, f32, f32, vp, vp, vp,
+                                                 i32, vp, i64, vp, vp, i32, i32]
         lib.oracle_ag_gemm.restype = i32
         lib.oracle_ag_gemm.argtypes = [i32, i64, i64, i64, f32, vp, vp, i32, vp, i64, vp, vp]
         lib.oracle_ag_schedule.restype = i64
@@ -75,11 +78,14 @@ def _u16(a: np.ndarray) -> np.ndarray:
 
 
 def gemm_rs(A: np.ndarray, B: np.ndarray, C: np.ndarray | None, alpha: float, beta: float,
-            y_dtype: str = "fp32", rows=None, threads: int | None = None) -> np.ndarray:
+            y_dtype: str = "fp32", rows=None, threads: int | None = None,
+            split: int = 0) -> np.ndarray:
     """Y (or the listed rows of Y) of the fused GEMM + reduce-scatter.
 
     A: uint16 [W, M, K/W] (bf16 bits); B: uint16 [W, K/W, N]; C: uint16 [M, N] or None.
     Returns float32 [rows, N] for y_dtype "fp32", uint16 bf16 bits for "bf16".
+    split = 0: the W partials are folded in rank order; 0 < split < W: the two-level
+    fold (ranks [0, split) and [split, W) each in rank order, then the two sums).
     """
     A, B = _u16(A), _u16(B)
     W, M, Kpr = A.shape
@@ -98,12 +104,12 @@ def gemm_rs(A: np.ndarray, B: np.ndarray, C: np.ndarray | None, alpha: float, be
     y_bf16 = 1 if y_dtype == "bf16" else 0
     out = np.empty((n_rows, N), dtype=np.uint16 if y_bf16 else np.float32)
     lib = _load()
-    rc = lib.oracle_gemm_rs(
+    rc = lib.oracle_gemm_rs_two_level(
         W, M, N, W * Kpr, ctypes.c_float(alpha), ctypes.c_float(beta),
         A.ctypes.data, B.ctypes.data, None if C is None else C.ctypes.data,
         y_bf16, None if rows_arr is None else rows_arr.ctypes.data, n_rows,
         None if y_bf16 else out.ctypes.data, out.ctypes.data if y_bf16 else None,
-        int(threads or 0))
+        int(threads or 0), int(split))
     if rc != 0:
         raise ValueError(f"oracle_gemm_rs rejected its arguments (rc={rc})")
     return out

@@ -85,13 +85,21 @@ void oracle_float_from_bf16(const uint16_t *x, float *out, int64_t n)
  * of Y.  A is [W][M][K/W] bf16, B is [W][K/W][N] bf16, C is [M][N] bf16
  * (ignored when beta == 0; may be NULL then).  The output is [n_rows][N]:
  * y_f32 when y_is_bf16 == 0, else y_bf16.
+ *
+ * split = 0: the fold over the ranks is one level, y = p_0, then y = y + p_r.
+ * 0 < split < W: two levels ("flux实现：sm80 gemm+rs", section "2D Ring优化": the
+ * ranks form two groups, each keeps its own partial sum, and the two are
+ * added last): y0 = fold of p_0 .. p_{split-1} and y1 = fold of
+ * p_split .. p_{W-1}, each in rank order, then y = y0 + y1.
  * Returns 0, or -1 on bad arguments.
  */
-int oracle_gemm_rs(int W, int64_t M, int64_t N, int64_t K, float alpha, float beta,
-                   const uint16_t *A, const uint16_t *B, const uint16_t *C,
-                   int y_is_bf16, const int64_t *rows, int64_t n_rows,
-                   float *y_f32, uint16_t *y_bf16, int n_threads)
+static int gemm_rs_impl(int W, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                        const uint16_t *A, const uint16_t *B, const uint16_t *C, int y_is_bf16,
+                        const int64_t *rows, int64_t n_rows, float *y_f32, uint16_t *y_bf16,
+                        int n_threads, int split)
 {
+    if (split < 0 || split >= W)
+        split = 0;
     if (W < 1 || M < 0 || N < 0 || K < 0 || K % W != 0 || M % W != 0)
         return -1;
     if (beta != 0.0f && C == NULL)
@@ -111,7 +119,8 @@ int oracle_gemm_rs(int W, int64_t M, int64_t N, int64_t K, float alpha, float be
     {
         double *s = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
         float *y = (float *)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
-        if (s == NULL || y == NULL) {
+        float *y1 = (float *)malloc((size_t)(N > 0 ? N : 1) * sizeof(float));
+        if (s == NULL || y == NULL || y1 == NULL) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -140,12 +149,21 @@ int oracle_gemm_rs(int W, int64_t M, int64_t N, int64_t K, float alpha, float be
                         if (beta != 0.0f)
                             v += (double)beta * (double)bf16_to_float(C[m * N + n]);
                         const float p = (float)v;
-                        if (r == 0)
+                        if (split > 0 && r >= split) {      /* the second group's own sum */
+                            if (r == split)
+                                y1[n] = p;
+                            else
+                                y1[n] = y1[n] + p;
+                        } else if (r == 0) {
                             y[n] = p;
-                        else
+                        } else {
                             y[n] = y[n] + p;
+                        }
                     }
                 }
+                if (split > 0)
+                    for (int64_t n = 0; n < N; ++n)
+                        y[n] = y[n] + y1[n];
                 for (int64_t n = 0; n < N; ++n) {
                     if (y_is_bf16)
                         y_bf16[ii * N + n] = float_to_bf16_rne(y[n]);
@@ -156,8 +174,28 @@ int oracle_gemm_rs(int W, int64_t M, int64_t N, int64_t K, float alpha, float be
         }
         free(s);
         free(y);
+        free(y1);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_gemm_rs(int W, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                   const uint16_t *A, const uint16_t *B, const uint16_t *C,
+                   int y_is_bf16, const int64_t *rows, int64_t n_rows,
+                   float *y_f32, uint16_t *y_bf16, int n_threads)
+{
+    return gemm_rs_impl(W, M, N, K, alpha, beta, A, B, C, y_is_bf16, rows, n_rows, y_f32, y_bf16,
+                        n_threads, 0);
+}
+
+/* The two-level fold: ranks [0, split) and [split, W) (see gemm_rs_impl). */
+int oracle_gemm_rs_two_level(int W, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                             const uint16_t *A, const uint16_t *B, const uint16_t *C,
+                             int y_is_bf16, const int64_t *rows, int64_t n_rows,
+                             float *y_f32, uint16_t *y_bf16, int n_threads, int split)
+{
+    return gemm_rs_impl(W, M, N, K, alpha, beta, A, B, C, y_is_bf16, rows, n_rows, y_f32, y_bf16,
+                        n_threads, split);
 }
 
 /*

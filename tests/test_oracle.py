@@ -159,6 +159,39 @@ def test_fold_is_in_rank_order():
     assert np.all(yr == 0.0)
 
 
+def test_two_level_fold_associates_by_group():
+    """p = (2^27, 1, -2^27, 1).  One level: ((2^27 + 1) + -2^27) + 1 = 1, since
+    2^27 + 1 rounds to 2^27.  Two levels of two ranks: (2^27 + 1) + (-2^27 + 1)
+    = 2^27 + -2^27 = 0.  The group sums are formed first, then added."""
+    W, M, N, Kpr = 4, 4, 1, 1
+    a = np.array([2.0 ** 14, 1.0, -(2.0 ** 14), 1.0], dtype=np.float32)
+    b = np.array([2.0 ** 13, 1.0, 2.0 ** 13, 1.0], dtype=np.float32)
+    A = np.zeros((W, M, Kpr), dtype=np.float32)
+    B = np.zeros((W, Kpr, N), dtype=np.float32)
+    for r in range(W):
+        A[r, :, 0] = a[r]
+        B[r, 0, 0] = b[r]
+    Ab, Bb = oracle.bf16_from_float(A), oracle.bf16_from_float(B)
+    assert np.all(oracle.gemm_rs(Ab, Bb, None, 1.0, 0.0, "fp32") == 1.0)
+    assert np.all(oracle.gemm_rs(Ab, Bb, None, 1.0, 0.0, "fp32", split=2) == 0.0)
+    # split 0 and out-of-range splits are the one-level fold
+    assert np.all(oracle.gemm_rs(Ab, Bb, None, 1.0, 0.0, "fp32", split=4) == 1.0)
+
+
+def test_two_level_fold_is_exact_on_integer_inputs():
+    """Integer-valued inputs make every partial sum exact, so any association
+    gives the one-level result bit for bit (here: int64 products)."""
+    rng = np.random.default_rng(9)
+    W, M, N, Kpr = 6, 12, 16, 24
+    A = rng.integers(-2, 3, (W, M, Kpr)).astype(np.float32)
+    B = rng.integers(-2, 3, (W, Kpr, N)).astype(np.float32)
+    ref = sum(A[r].astype(np.int64) @ B[r].astype(np.int64) for r in range(W)).astype(np.float32)
+    Ab, Bb = oracle.bf16_from_float(A), oracle.bf16_from_float(B)
+    for split in (0, 1, 3, 5):
+        np.testing.assert_array_equal(oracle.gemm_rs(Ab, Bb, None, 1.0, 0.0, "fp32", split=split),
+                                      ref)
+
+
 def test_bf16_conversion_matches_torch_rne():
     g = torch.Generator().manual_seed(5)
     x = torch.randn(200000, generator=g) * 1000
