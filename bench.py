@@ -543,11 +543,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     cold_ms = sorted(a.elapsed_time(b) for a, b in zip(cs, ce))
 
-    # the other reduction of the library: last-arriver (rank-order fold)
+    # the library's other reductions: last-arriver (rank-order fold) and the
+    # two-level fold (two rank groups, then their sums)
     other_mode = {}
     mode0 = op.plan["reduce_mode"]
     for mode, name in ((binding.GEMM_RS_REDUCE_LAST_ARRIVER, "last_arriver"),
-                       (binding.GEMM_RS_REDUCE_CHAIN, "chain")):
+                       (binding.GEMM_RS_REDUCE_CHAIN, "chain"),
+                       (binding.GEMM_RS_REDUCE_TWO_LEVEL, "two_level")):
         if mode == mode0:
             continue
         binding.gemm_rs_set_reduce_mode(op.handle, mode)

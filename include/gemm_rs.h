@@ -95,7 +95,15 @@ enum {
     GEMM_RS_REDUCE_CHAIN = 0,
     /* Every rank stores its partial.  The last rank to arrive at a tile folds
      * all W partials in rank order 0 .. W-1 and writes Y. */
-    GEMM_RS_REDUCE_LAST_ARRIVER = 1
+    GEMM_RS_REDUCE_LAST_ARRIVER = 1,
+    /* The two-level reduction of a multi-node reduce-scatter, as one GPU sees
+     * it ("flux实现：sm80 gemm+rs", section "2D Ring优化": the partial sums of
+     * the ranks of one node meet first, and the nodes' sums meet after that).
+     * The ranks form two groups, [0, h) and [h, W) with h = ceil(W/2).  Each
+     * group folds its ranks in rank order as in CHAIN, into a running sum of
+     * its own.  The group that finishes second writes
+     * Y = (sum of group 0) + (sum of group 1).  W = 1 is CHAIN. */
+    GEMM_RS_REDUCE_TWO_LEVEL = 2
 };
 
 /* The order in which the W logical ranks' tiles run (gemm_rs_set_schedule). */
@@ -119,7 +127,8 @@ enum {
  * covers every tile width the library may pick.  Layout (internal, for
  * information):
  *   [0, 256)   device status word
- *   flags      one uint32 arrival counter per output tile (ceil(M/128) x ceil(N/64) max)
+ *   flags      three uint32 state words per output tile (ceil(M/128) x ceil(N/64) tiles
+ *              max): a chain state or arrival counter per rank group, and a group count
  *   partials   fp32 partial tiles, one per (output tile, rank), grouped by the chunk
  *              that owns the tile's first row: W * ceil(M/128)*128 * ceil(N/256)*256 * 4 bytes
  * Returns 0 for invalid arguments (same checks as gemm_rs_create).
@@ -226,7 +235,7 @@ GEMM_RS_API int64_t gemm_rs_schedule(int64_t M, int64_t N, int W, int bm, int bn
  *   grid     CTAs launched (persistent: one per SM, at most one per work item)
  *   colgroup, rowgroup, rank_order  the schedule in effect (see gemm_rs_set_schedule;
  *                       rank_order is GEMM_RS_RANKS_SEQUENTIAL or _INTERLEAVED)
- *   reduce_mode         GEMM_RS_REDUCE_CHAIN or GEMM_RS_REDUCE_LAST_ARRIVER
+ *   reduce_mode         GEMM_RS_REDUCE_* in effect
  */
 GEMM_RS_API int gemm_rs_get_plan(gemm_rs_t h, int *bm, int *bn, int *stages, int *grid,
                                  int *colgroup, int *rowgroup, int *rank_order, int *reduce_mode);
@@ -267,11 +276,12 @@ GEMM_RS_API int gemm_rs_set_tile(gemm_rs_t h, int bm, int bn);
  * Returns ERR_ARG for negative values or an unknown rank order. */
 GEMM_RS_API int gemm_rs_set_schedule(gemm_rs_t h, int colgroup, int rowgroup, int rank_order);
 
-/* Select the reduction (GEMM_RS_REDUCE_*).  Both give Y within the stated
+/* Select the reduction (GEMM_RS_REDUCE_*).  All give Y within the stated
  * tolerances of each other.  Each is bit-identical from run to run.  They
  * differ in summation order: rank order 0..W-1 for LAST_ARRIVER, the
  * schedule's arrival order for CHAIN (the same rank order with the default
- * sequential ranks).  CHAIN adds the middle positions to the running sum in L2
+ * sequential ranks), rank order within each of the two groups for TWO_LEVEL.
+ * CHAIN and TWO_LEVEL add the middle positions to the running sum in L2
  * (red.add.f32), which flushes subnormal sums to zero.  ERR_ARG for other
  * values. */
 GEMM_RS_API int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode);

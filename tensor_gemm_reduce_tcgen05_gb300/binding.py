@@ -37,6 +37,7 @@ GEMM_RS_DEBUG_STALL_PRODUCER = 1
 
 GEMM_RS_REDUCE_CHAIN = 0
 GEMM_RS_REDUCE_LAST_ARRIVER = 1
+GEMM_RS_REDUCE_TWO_LEVEL = 2
 GEMM_RS_RANKS_DEFAULT = 0
 GEMM_RS_RANKS_SEQUENTIAL = 1
 GEMM_RS_RANKS_INTERLEAVED = 2
@@ -289,10 +290,10 @@ class GemmRS:
         gemm_rs_reset(self.handle, _stream_ptr(stream))
 
     def flags_view(self):
-        """The tile counters (a view into the workspace), for tests."""
+        """The tile state words (a view into the workspace), for tests."""
         import torch
         nM, nN = -(-self.M // 128), -(-self.N // 64)
-        return self.workspace[256:256 + 4 * nM * nN].view(torch.int32)
+        return self.workspace[256:256 + 3 * 4 * nM * nN].view(torch.int32)
 
     def close(self) -> None:
         if getattr(self, "handle", None) is not None:

@@ -33,7 +33,10 @@ Layout layout_for(int64_t M, int64_t N, int W)
     Layout L;
     const int64_t nM = cdiv(M, gemm_rs::kBM);
     L.flags_off = kStatusBytes;
-    L.flags_bytes = round_up(static_cast<size_t>(nM * cdiv(N, 64)) * sizeof(uint32_t), 256);
+    // three state words per output tile: the chain (or arrival counter) of
+    // ranks [0, W) or of the first group of the two-level fold, the second
+    // group's chain, and the count of groups done
+    L.flags_bytes = round_up(static_cast<size_t>(3 * nM * cdiv(N, 64)) * sizeof(uint32_t), 256);
     L.part_off = L.flags_off + L.flags_bytes;
     L.part_bytes = static_cast<size_t>(W) * static_cast<size_t>(nM) * gemm_rs::kBM *
                    static_cast<size_t>(cdiv(N, 256) * 256) * sizeof(float);
@@ -266,7 +269,7 @@ struct gemm_rs_s {
     int colgroup; // 0: the default (pick_colgroup)
     int rowgroup; // 0: the default (pick_rowgroup)
     int rank_order; // GEMM_RS_RANKS_*
-    int reduce_mode; // GEMM_RS_REDUCE_CHAIN (default) or GEMM_RS_REDUCE_LAST_ARRIVER
+    int reduce_mode; // GEMM_RS_REDUCE_* (default CHAIN)
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
     unsigned long long timeout;
@@ -496,7 +499,8 @@ int gemm_rs_set_reduce_mode(gemm_rs_t h, int mode)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
-    if (mode != GEMM_RS_REDUCE_CHAIN && mode != GEMM_RS_REDUCE_LAST_ARRIVER)
+    if (mode != GEMM_RS_REDUCE_CHAIN && mode != GEMM_RS_REDUCE_LAST_ARRIVER &&
+        mode != GEMM_RS_REDUCE_TWO_LEVEL)
         return fail(GEMM_RS_ERR_ARG, "unknown reduce mode %d", mode);
     h->reduce_mode = mode;
     return GEMM_RS_OK;
@@ -569,7 +573,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
         return fail(GEMM_RS_ERR_ARG, "handle was created on device %d, current device is %d",
                     h->device, dev);
 
-    gemm_rs::KernelArgs a;
+    gemm_rs::KernelArgs a{};
     a.W = h->W;
     a.M = static_cast<int>(h->M);
     a.N = static_cast<int>(h->N);
@@ -579,7 +583,9 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.nMs = static_cast<int>(cdiv(h->M, h->bm));
     a.colgroup = colgroup_of(h);
     a.rowgroup = rowgroup_of(h);
-    a.chain = h->reduce_mode == GEMM_RS_REDUCE_CHAIN ? 1 : 0;
+    a.chain = h->reduce_mode != GEMM_RS_REDUCE_LAST_ARRIVER ? 1 : 0;
+    // two groups of ranks, [0, ceil(W/2)) and [ceil(W/2), W)
+    a.split = (h->reduce_mode == GEMM_RS_REDUCE_TWO_LEVEL && h->W > 1) ? (h->W + 1) / 2 : 0;
     a.seq = sequential(h) ? 1 : 0;
     // Sequential ranks reach a tile a rank's pass apart, and a single row tile
     // brings all positions at once: neither gains from waiting for a turn.
@@ -838,7 +844,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
         return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
 
     const int bn = pick_bn(M, N, W, sms);
-    gemm_rs::KernelArgs a;
+    gemm_rs::KernelArgs a{};
     a.W = W;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -851,6 +857,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.chain = 1;
     a.seq = 1;
     a.chain_wait = 0;
+    a.split = 0;
     a.R = M / W;
     a.total = static_cast<int64_t>(W) * a.nM * a.nN;
     a.alpha = alpha;

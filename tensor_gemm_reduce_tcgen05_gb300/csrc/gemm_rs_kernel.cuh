@@ -113,6 +113,8 @@ struct KernelArgs {
     int chain;      // 1: chain reduction (in-order fold as tiles land), 0: last arriver reduces
     int seq;        // 1: the ranks' tiles one rank after another, 0: the ranks side by side
     long long chain_wait; // SM cycles a chain position waits for its turn before storing
+    int split;      // chain mode, two-level fold: ranks [0, split) and [split, W) fold
+                    // separately, then the two sums are added (0: one fold over all W)
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -140,6 +142,7 @@ struct SmemCtl {
     int epi_direct[2]; // chain mode: the epilogue owns the fold of the tile in TMEM buffer b
     int epi_fold;      // chain mode: position the epilogue folds on from (-1: none)
     int epi_fold_end;  // chain mode: last stored position of the current fold
+    int epi_combine;   // two-level fold: this CTA adds the two groups' sums into Y
     uint32_t tmem_base;
     int abort;
 };
@@ -345,17 +348,18 @@ __device__ __forceinline__ bool rq_push(const KernelArgs &a, SmemCtl *ctl, uint3
     return true;
 }
 
-// y = slot[0] + slot[f] + slot[f+1] + ... + slot[hi] with f = max(lo, 1),
+// y = slot[b] + slot[f] + slot[f+1] + ... + slot[hi] with f = max(lo, b+1),
 // folded left to right in fp32, for the 32-column slabs slab0 .. slab1-1 of
-// one quarter (32 rows) of tile `tile`, by one warp (lane = row).  Slot 0
-// holds the running sum (chain mode) or rank 0's partial (last-arriver mode,
-// lo = 0: the W partials in rank order).  to_y: convert and write Y.
-// Otherwise the sum is written back to slot 0.  The slots f .. hi (and slot 0
+// one quarter (32 rows) of tile `tile`, by one warp (lane = row).  Slot b
+// holds a running sum (chain mode: b = 0, or the first slot of the second
+// rank group in the two-level fold) or rank 0's partial (last-arriver mode,
+// b = lo = 0: the W partials in rank order).  to_y: convert and write Y.
+// Otherwise the sum is written back to slot b.  The slots f .. hi (and slot b
 // after writing Y) are dead afterwards, so their L2 lines are dropped without
 // write-back.
 template <int BN>
-__device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int q, int lane, int lo,
-                                             int hi, bool to_y, int slab0, int slab1)
+__device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int q, int lane, int b,
+                                             int lo, int hi, bool to_y, int slab0, int slab1)
 {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::kSlabs;
@@ -364,14 +368,16 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
     const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
     const bool row_ok = m < a.M;
     // slot 0's 32-row quarter; slot s's is s * kSlotFloats further on
-    float *qb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
+    float *q0 = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                 static_cast<int64_t>(q) * S * 1024;
-    const int first = lo > 1 ? lo : 1;
+    float *qb = q0 + static_cast<int64_t>(b) * Cfg::kSlotFloats; // slot b
+    const int first = lo > b + 1 ? lo : b + 1;
 #pragma unroll 1
     for (int slab = slab0; slab < slab1; ++slab) {
         // One slab of a slot is 8 float4 per lane (a 4 KB block per warp),
         // loaded at once.  Fixed order: y = slot[0], then y = y + slot[s].
         const float *sb = qb + slab * 1024 + lane * 4;
+        const float *s0 = q0 + slab * 1024 + lane * 4;
         float4 y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -383,11 +389,11 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
             float4 u[8], w2[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                u[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(sl) * Cfg::kSlotFloats + j * 128);
+                u[j] = ptx::ld_cg_f4(s0 + static_cast<int64_t>(sl) * Cfg::kSlotFloats + j * 128);
             if (two) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    w2[j] = ptx::ld_cg_f4(sb + static_cast<int64_t>(sl + 1) * Cfg::kSlotFloats + j * 128);
+                    w2[j] = ptx::ld_cg_f4(s0 + static_cast<int64_t>(sl + 1) * Cfg::kSlotFloats + j * 128);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -420,7 +426,7 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
         if (to_y)
             ptx::discard_l2_line(qb + slab * 1024 + lane * 32);
         for (int s = first; s <= hi; ++s)
-            ptx::discard_l2_line(qb + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 +
+            ptx::discard_l2_line(q0 + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 +
                                  lane * 32);
     }
 }
@@ -498,6 +504,20 @@ __device__ __forceinline__ bool chain_wait_own(uint32_t *flag, uint32_t i, long 
     }
 }
 
+// Two-level fold: a rank group has folded all its positions (its sum is in
+// its first slot, published by the caller's barrier and this atomic's release
+// side).  The groups count themselves in on the tile's third state word; the
+// second to arrive returns 1, puts the word back to 0 for the next call, and
+// adds the two sums.
+__device__ __forceinline__ int group_done(const KernelArgs &a, int tile)
+{
+    uint32_t *done = a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile;
+    if (ptx::atom_add_acq_rel_gpu(done, 1u) == 0u)
+        return 0;
+    ptx::st_relaxed_gpu(done, 0u);
+    return 1;
+}
+
 // A consumer warp: claim entries until it takes a stop entry.  Entry kinds:
 //   (tile << 2) | q   last-arriver mode: fold all W slots of quarter q into Y
 //   -1                stop
@@ -527,7 +547,7 @@ __device__ __forceinline__ void run_consumer(const KernelArgs &a, SmemCtl *ctl, 
         }
         if (entry < 0)
             break;
-        fold_quarter<BN>(a, entry >> 2, entry & 3, lane, 0, a.W - 1, true, 0, TileCfg<BN>::kSlabs);
+        fold_quarter<BN>(a, entry >> 2, entry & 3, lane, 0, 0, a.W - 1, true, 0, TileCfg<BN>::kSlabs);
     }
 }
 
@@ -578,11 +598,20 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         const bool half_ok = mt < a.nM; // a pair's second half may lie wholly below M
         const int tile = mt * a.nN + nt;
         const int buf = it & 1;
+        // The chain this contribution joins.  One fold over all W ranks at
+        // position pos, or, for the two-level fold, the fold of its rank group
+        // (ranks [0, split) or [split, W)) at its place in the group, with the
+        // group's own state word and its running sum in the group's first slot.
+        const int grp = (a.split > 0 && r >= a.split) ? 1 : 0;
+        const int base = grp ? a.split : 0;
+        const int cpos = a.split > 0 ? r - base : pos;
+        const int clen = a.split > 0 ? (grp ? a.W - a.split : a.split) : a.W;
+        uint32_t *cflag = a.flags + static_cast<int64_t>(grp) * a.nM * a.nN + tile;
         // Chain mode: try to take the fold while the accumulator is still being
         // computed, so the decision is ready when it lands.
         if (etid == 0)
             ctl->epi_direct[buf] =
-                (a.chain && half_ok && chain_try_own(a.flags + tile, static_cast<uint32_t>(pos))) ? 1 : 0;
+                (a.chain && half_ok && chain_try_own(cflag, static_cast<uint32_t>(cpos))) ? 1 : 0;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
         const uint32_t fb = ptx::smem_u32(&ctl->acc_full[buf]);
         const bool waited = PAIR ? ptx::mbar_wait_cluster(fb, aph, a.timeout, abort_flag)
@@ -593,9 +622,17 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         // column group with the ranks side by side, whose B panels are not in
         // L2 yet).  Where positions land together, storing at once and folding
         // once is cheaper than a queue of waits.
-        if (etid == 0 && a.chain && waited && half_ok && ctl->epi_direct[buf] == 0)
-            ctl->epi_direct[buf] =
-                chain_wait_own(a.flags + tile, static_cast<uint32_t>(pos), a.chain_wait) ? 1 : 0;
+        if (etid == 0 && a.chain && waited && half_ok) {
+            if (ctl->epi_direct[buf] == 0)
+                ctl->epi_direct[buf] =
+                    chain_wait_own(cflag, static_cast<uint32_t>(cpos), a.chain_wait) ? 1 : 0;
+            // Two-level fold, last position of a group: if the other group is
+            // already done, this position adds all three terms and writes Y
+            // (direct = 2) instead of publishing its group's sum.
+            if (a.split > 0 && ctl->epi_direct[buf] != 0 && cpos == clen - 1 &&
+                ptx::ld_acquire_gpu(a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile) != 0u)
+                ctl->epi_direct[buf] = 2;
+        }
         if (ptx::named_bar_or(kBarEpi, nthr, !(waited && ok))) {
             ok = false;
             break;
@@ -612,14 +649,20 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             }
             continue;
         }
-        const bool direct = *reinterpret_cast<volatile int *>(&ctl->epi_direct[buf]) != 0;
-        // Chain mode: the running sum lives in slot 0.  Position 0 stores it,
-        // positions 1 .. W-2 add to it in L2, and the last position reads it
-        // and writes Y.  An early position stores its partial in its own slot.
-        const int sidx = a.chain ? (direct ? 0 : pos) : r; // slot written
-        const bool to_y = direct && pos == a.W - 1;        // the last fold writes Y
-        const bool add_prev = to_y && pos > 0;             // read the running sum
-        const bool add_l2 = direct && pos > 0 && !to_y;    // add to it in L2
+        const int dmode = *reinterpret_cast<volatile int *>(&ctl->epi_direct[buf]);
+        const bool direct = dmode != 0;
+        const bool final = dmode == 2; // two-level: the other group's sum is ready
+        // Chain mode: the running sum lives in slot `base`.  Position 0 stores
+        // it, the middle positions add to it in L2, and the last position of a
+        // one-level fold reads it and writes Y.  The last position of a group
+        // of the two-level fold adds to it like the middle ones, unless the
+        // other group is done: then it reads both sums and writes
+        // Y = (other group's sum) + (running sum + partial).  An early
+        // position stores its partial in its own slot.
+        const int sidx = a.chain ? (direct ? base : base + cpos) : r; // slot written
+        const bool to_y = direct && (a.split == 0 || final) && cpos == clen - 1;
+        const bool add_prev = to_y && cpos > 0;                      // read the running sum
+        const bool add_l2 = direct && cpos > 0 && !to_y;             // add to it in L2
 
         const int64_t m = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
         const bool row_ok = m < a.M;
@@ -628,7 +671,9 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         float *tb = a.part + static_cast<int64_t>(tile) * a.W * Cfg::kSlotFloats +
                     static_cast<int64_t>(q) * Cfg::kSlabs * 1024 + lane * 4;
         float *slot = tb + static_cast<int64_t>(sidx) * Cfg::kSlotFloats;
-        const float *prev = tb; // slot 0: the running sum
+        const float *prev = tb + static_cast<int64_t>(base) * Cfg::kSlotFloats; // running sum
+        // the other group's sum (two-level, final position)
+        const float *other = tb + static_cast<int64_t>(grp ? 0 : a.split) * Cfg::kSlotFloats;
         if (!q_live) {
             ptx::tc_fence_before();
             __syncwarp();
@@ -701,6 +746,20 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     p[4 * j + 3] = rs[j].w + p[4 * j + 3];
                 }
             }
+            if (final) {
+                // then the other group's sum (fp32 addition is commutative, so
+                // this is y0 + y1 whichever group finishes second)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    rs[j] = ptx::ld_cg_f4(other + slab * 1024 + j * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    p[4 * j] = rs[j].x + p[4 * j];
+                    p[4 * j + 1] = rs[j].y + p[4 * j + 1];
+                    p[4 * j + 2] = rs[j].z + p[4 * j + 2];
+                    p[4 * j + 3] = rs[j].w + p[4 * j + 3];
+                }
+            }
             if (to_y) {
                 const int64_t n0 = static_cast<int64_t>(nt) * BN + slab * 32;
 #pragma unroll
@@ -726,10 +785,13 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                                     make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]),
                                     st_pol);
             }
-            if (add_prev) {
-                // the running sum is dead: drop its lines of this warp's 4 KB block
+            if (add_prev || final) {
+                // the sums read are dead: drop their lines of this warp's 4 KB block
                 __syncwarp();
-                ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
+                if (add_prev)
+                    ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
+                if (final)
+                    ptx::discard_l2_line(other - lane * 4 + slab * 1024 + lane * 32);
             }
         }
 
@@ -739,8 +801,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         // barrier its CTA, then sees them.
         ptx::named_bar_sync(kBarEpi, nthr);
         if (etid == 0) {
-            uint32_t *flag = a.flags + tile;
             if (!a.chain) {
+                uint32_t *flag = a.flags + tile;
                 const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
                 if (old == static_cast<uint32_t>(a.W - 1)) {
                     // Last arriver: the counter goes back to 0 for the next call
@@ -751,61 +813,79 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                             ok = rq_push(a, ctl, rq_n, (tile << 2) | qq);
                 }
             } else {
-                int fold_from = -1;
+                int fold_from = -1, combine = 0;
                 if (direct) {
-                    if (to_y)
-                        ptx::st_relaxed_gpu(flag, 0u); // back to 0 for the next call
-                    else if (chain_pass_on(flag, static_cast<uint32_t>(pos + 1),
-                                           (static_cast<uint32_t>(pos) << 16) | kChainOwn))
-                        fold_from = pos + 1;
+                    if (cpos == clen - 1) {
+                        ptx::st_relaxed_gpu(cflag, 0u); // back to 0 for the next call
+                        if (final) // Y is written; the group count goes back to 0
+                            ptx::st_relaxed_gpu(a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile, 0u);
+                        else if (a.split > 0)
+                            combine = group_done(a, tile);
+                    } else if (chain_pass_on(cflag, static_cast<uint32_t>(cpos + 1),
+                                             (static_cast<uint32_t>(cpos) << 16) | kChainOwn)) {
+                        fold_from = cpos + 1;
+                    }
                 } else {
-                    const uint32_t old = ptx::atom_or_acq_rel_gpu(flag, 1u << pos);
-                    if (chain_k(old) == static_cast<uint32_t>(pos) && !(old & kChainOwn) &&
-                        chain_try_own(flag, static_cast<uint32_t>(pos)))
-                        fold_from = pos;
+                    const uint32_t old = ptx::atom_or_acq_rel_gpu(cflag, 1u << cpos);
+                    if (chain_k(old) == static_cast<uint32_t>(cpos) && !(old & kChainOwn) &&
+                        chain_try_own(cflag, static_cast<uint32_t>(cpos)))
+                        fold_from = cpos;
                 }
                 ctl->epi_fold = fold_from;
+                ctl->epi_combine = combine;
             }
         }
         if (a.chain) {
             // Fold on while the positions after the running sum are already
-            // stored: every warp takes its own slabs of its quarter.
+            // stored, then, for the two-level fold, add the two groups' sums if
+            // this CTA completed the second group.  A fold reads only global
+            // memory, so the (quarter, slab) units of the live quarters are
+            // spread over all epilogue warps.
             ptx::named_bar_sync(kBarEpi, nthr);
             int k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
-            while (k >= 0) {
-                uint32_t *flag = a.flags + tile;
-                if (etid == 0) {
-                    const uint32_t st = ptx::ld_acquire_gpu(flag);
-                    int j = k;
-                    while (j + 1 < a.W && ((st >> (j + 1)) & 1u))
-                        ++j;
-                    ctl->epi_fold_end = j;
+            bool combine = *reinterpret_cast<volatile int *>(&ctl->epi_combine) != 0;
+            while (k >= 0 || combine) {
+                int fb = 0, flo = a.split, fhi = a.split; // the combine: y = slot[0] + slot[split]
+                bool fy = true, last = false;
+                if (k >= 0) {
+                    if (etid == 0) {
+                        const uint32_t st = ptx::ld_acquire_gpu(cflag);
+                        int j = k;
+                        while (j + 1 < clen && ((st >> (j + 1)) & 1u))
+                            ++j;
+                        ctl->epi_fold_end = j;
+                    }
+                    ptx::named_bar_sync(kBarEpi, nthr);
+                    const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
+                    last = j == clen - 1;
+                    fb = base;
+                    flo = base + k;
+                    fhi = base + j;
+                    fy = last && a.split == 0;
                 }
-                ptx::named_bar_sync(kBarEpi, nthr);
-                const int j = *reinterpret_cast<volatile int *>(&ctl->epi_fold_end);
-                // A fold reads only global memory, so the (quarter, slab) units
-                // of the live quarters are spread over all epilogue warps.
-                {
-                    const int64_t rows_left = a.M - static_cast<int64_t>(mt) * kBM;
-                    const int nlive = rows_left >= kBM ? 4 : static_cast<int>((rows_left + 31) / 32);
-                    const int units = nlive * Cfg::kSlabs;
-                    const int nw = nthr / 32;
-                    for (int u = (warp - kEpiWarp0); u < units; u += nw)
-                        fold_quarter<BN>(a, tile, u / Cfg::kSlabs, lane, k, j, j == a.W - 1,
-                                         u % Cfg::kSlabs, u % Cfg::kSlabs + 1);
-                }
+                const int64_t rows_left = a.M - static_cast<int64_t>(mt) * kBM;
+                const int nlive = rows_left >= kBM ? 4 : static_cast<int>((rows_left + 31) / 32);
+                for (int u = (warp - kEpiWarp0); u < nlive * Cfg::kSlabs; u += nthr / 32)
+                    fold_quarter<BN>(a, tile, u / Cfg::kSlabs, lane, fb, flo, fhi, fy, u % Cfg::kSlabs,
+                                     u % Cfg::kSlabs + 1);
+                if (k < 0)
+                    break; // the combine wrote Y
                 ptx::named_bar_sync(kBarEpi, nthr);
                 if (etid == 0) {
                     int next = -1;
-                    if (j == a.W - 1)
-                        ptx::st_relaxed_gpu(flag, 0u);
-                    else if (chain_pass_on(flag, static_cast<uint32_t>(j + 1),
-                                           ptx::ld_acquire_gpu(flag)))
-                        next = j + 1;
+                    if (last) {
+                        ptx::st_relaxed_gpu(cflag, 0u);
+                        if (a.split > 0)
+                            ctl->epi_combine = group_done(a, tile);
+                    } else if (chain_pass_on(cflag, static_cast<uint32_t>(fhi - base + 1),
+                                             ptx::ld_acquire_gpu(cflag))) {
+                        next = fhi - base + 1;
+                    }
                     ctl->epi_fold = next;
                 }
                 ptx::named_bar_sync(kBarEpi, nthr);
                 k = *reinterpret_cast<volatile int *>(&ctl->epi_fold);
+                combine = *reinterpret_cast<volatile int *>(&ctl->epi_combine) != 0;
             }
         }
     }

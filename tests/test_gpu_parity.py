@@ -31,7 +31,7 @@ SHAPES = [
 TILES = [(128, 256), (128, 128), (128, 64), (256, 256)]  # (256, 256): the CTA-pair kernel
 
 
-MODES = [0, 1]  # GEMM_RS_REDUCE_CHAIN, GEMM_RS_REDUCE_LAST_ARRIVER
+MODES = [0, 1, 2]  # GEMM_RS_REDUCE_CHAIN, _LAST_ARRIVER, _TWO_LEVEL
 
 
 ORDERS = [1, 2]  # GEMM_RS_RANKS_SEQUENTIAL (the default), GEMM_RS_RANKS_INTERLEAVED
@@ -208,7 +208,7 @@ def test_timeout_path_reports_and_recovers(tile):
 
 
 def test_reduce_modes_agree_and_each_is_deterministic():
-    """Both reductions and both rank orders on one shape with many tiles per
+    """All reductions and both rank orders on one shape with many tiles per
     chunk: each is bit-identical across calls, and all agree within the fp32
     tolerance (they differ only in summation order).  With the ranks one after
     another, the chain folds in rank order, the last arriver's order."""
