@@ -348,6 +348,43 @@ def chunked_baseline(W, M, N, alpha, beta, y_code, Ad, Bd, Cd, Y, stream, dev):
 
 # --------------------------------------------------------------------------- our arm
 def time_loop(fn, steps, stream):
+    """Mean ms per call over `steps` calls of fn on `stream`.  Each call is
+    bracketed by its own event pair, the pattern of the fused arm's timed
+    region (whose per-call events give the kernel durations), so every arm
+    pays the same event overhead between calls."""
+    import torch
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    per_call = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(steps)]
+    torch.cuda.synchronize()
+    s.record(stream)
+    for a, b in per_call:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps
+
+
+def interleaved(arms, rounds, n, stream, timer=None):
+    """Mean ms per call of each arm ({name: fn}), timed in `rounds` rounds of
+    n calls per arm, the arms' order reversed every other round.  Under the
+    board's power cap the clock drifts down as a run goes on, so arms timed one
+    after the other are not comparable; interleaved rounds see the same clocks."""
+    timer = timer or time_loop
+    names = list(arms)
+    per = {k: [] for k in names}
+    for r in range(rounds):
+        for k in (names if r % 2 == 0 else names[::-1]):
+            per[k].append(timer(arms[k], n, stream))
+    return {k: sum(v) / len(v) for k, v in per.items()}
+
+
+def time_loop_b2b(fn, steps, stream):
+    """Mean ms per call with the calls back to back (no events between them):
+    what a caller that issues them in a row sees."""
     import torch
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
@@ -358,6 +395,28 @@ def time_loop(fn, steps, stream):
     e.record(stream)
     torch.cuda.synchronize()
     return s.elapsed_time(e) / steps
+
+
+def profile_unfused(args, w, Ad, Bd, Cd, Y, stream):
+    """Profiling run of the unfused arm alone: batched per-rank cuBLAS GEMMs into
+    fp32 partials, then the separate reduce kernel, warm-up + steps calls."""
+    import torch
+    from tensor_gemm_reduce_tcgen05_gb300 import binding
+    P = torch.empty((w.W, w.M, w.N), dtype=torch.float32, device=Ad.device)
+    y_code = binding.GEMM_RS_BF16 if w.y_dtype == "bf16" else binding.GEMM_RS_FP32
+
+    def unfused():
+        torch.bmm(Ad, Bd, out_dtype=torch.float32, out=P)
+        binding.gemm_rs_reduce_partials(P.data_ptr(), binding.GEMM_RS_FP32,
+                                        0 if Cd is None else Cd.data_ptr(), Y.data_ptr(), w.M, w.N,
+                                        w.W, w.alpha, w.beta, y_code, stream.cuda_stream)
+    for _ in range(args.warmup):
+        unfused()
+    ms = time_loop(unfused, args.steps, stream)
+    print(json.dumps({"metric": METRIC, "arm": "unfused", "ms_per_step": ms,
+                      "config": workload_config(w),
+                      "note": "profiling run: unfused arm only (torch.bmm fp32 out + reduce kernel)"}))
+    return 0
 
 
 def run_ours(args):
@@ -384,6 +443,8 @@ def run_ours(args):
         binding.gemm_rs_set_tile_n(op.handle, args.tile_n)
     Y = op.new_output()
     Y_pin = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+    if args.unfused_only:
+        return profile_unfused(args, w, Ad, Bd, Cd, Y, stream)
 
     def step():
         op.run(Ad, Bd, Cd, Y, stream)
@@ -495,18 +556,26 @@ def run_ours(args):
 
     for _ in range(max(3, args.warmup)):
         unfused()
-    unfused_ms = time_loop(unfused, args.steps, stream)
+    # fused and unfused in interleaved rounds (the same clocks for both)
+    rounds, per_round = 4, max(3, args.steps // 4)
+    pair = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream)
+    unfused_ms = pair["unfused"]
     gemms_ms = time_loop(gemms, args.steps, stream)
     reduce_ms = time_loop(reduce_only, args.steps, stream)
+    b2b = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream,
+                      timer=time_loop_b2b)
+    b2b = {"fused_ms": b2b["fused"], "unfused_ms": b2b["unfused"],
+           "fused_speedup": b2b["unfused"] / b2b["fused"]}
     del P
 
     # chunked two-stream baseline (async-TP style)
     chunked = chunked_baseline(w.W, w.M, w.N, w.alpha, w.beta, y_code, Ad, Bd, Cd, Y, stream, dev)
-    chunked_ms = None
+    chunked_ms = chunked_fused_ms = None
     if p_dtype == binding.GEMM_RS_FP32:
         for _ in range(max(3, args.warmup)):
             chunked()
-        chunked_ms = time_loop(chunked, args.steps, stream)
+        cp = interleaved({"fused": step, "chunked": chunked}, rounds, per_round, stream)
+        chunked_ms, chunked_fused_ms = cp["chunked"], cp["fused"]
     del chunked
 
     # full-K GEMM of the same shape (no reduce-scatter at all): context
@@ -607,10 +676,13 @@ def run_ours(args):
             "unfused": {"ms_per_step": unfused_ms,
                         "value": w.flops / (unfused_ms / 1e3) / 1e12,
                         "gemms_ms": gemms_ms, "reduce_ms": reduce_ms, "partials": partials_note,
-                        "fused_speedup": unfused_ms / ms_step},
+                        "fused_ms_interleaved": pair["fused"],
+                        "fused_speedup": unfused_ms / pair["fused"],
+                        "note": f"fused and unfused timed in {rounds} interleaved rounds of "
+                                f"{per_round} calls each, order reversed every round"},
             "unfused_chunked": None if chunked_ms is None else {
                 "ms_per_step": chunked_ms, "value": w.flops / (chunked_ms / 1e3) / 1e12,
-                "chunks": w.W, "fused_speedup": chunked_ms / ms_step,
+                "chunks": w.W, "fused_speedup": chunked_ms / chunked_fused_ms,
                 "note": "per chunk: W per-rank bmm (fp32 out) on one stream, reduce of the "
                         "previous chunk on a second stream, two chunk buffers"},
             "full_k_gemm": {"ms": fullk_ms, "value": w.flops / (fullk_ms / 1e3) / 1e12,
@@ -621,6 +693,8 @@ def run_ours(args):
             "ablation": {"kernel_batched_ms": ms_step, "kernel_sync_ms": ks_ms,
                          "clear_kernel_sync_ms": cks_ms},
             "other_reduce_mode": other_mode,
+            "back_to_back": dict(b2b, note="calls issued in a row with no events between "
+                                 "them; every other figure brackets each call with events"),
             "plan": plan,
         }
         print(json.dumps(line))
@@ -720,7 +794,9 @@ def run_ag(args):
         unfused()
         unfused_chunks()
         plain()
-    unfused_ms = time_loop(unfused, args.steps, stream)
+    rounds, per_round = 4, max(3, args.steps // 4)
+    pair = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream)
+    unfused_ms = pair["unfused"]
     gather_ms = time_loop(gather, args.steps, stream)
     chunks_ms = time_loop(unfused_chunks, args.steps, stream)
     plain_ms = time_loop(plain, args.steps, stream)
@@ -760,9 +836,10 @@ def run_ag(args):
         "kernel_ms_median": kernel_ms[len(kernel_ms) // 2], "kernel_ms_min": kernel_ms[0],
         "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": cpu,
         "unfused": {"ms_per_step": unfused_ms, "value": w.flops / (unfused_ms / 1e3) / 1e12,
-                    "gather_ms": gather_ms, "fused_speedup": unfused_ms / ms_step,
+                    "gather_ms": gather_ms, "fused_ms_interleaved": pair["fused"],
+                    "fused_speedup": unfused_ms / pair["fused"],
                     "note": "the all-gather as one copy of X into every rank's buffer, then "
-                            "torch.bmm"},
+                            "torch.bmm; fused and unfused timed in interleaved rounds"},
         "unfused_chunk_copies": {"ms_per_step": chunks_ms,
                                  "value": w.flops / (chunks_ms / 1e3) / 1e12,
                                  "note": "W*(W-1) chunk copies (one per rank and remote chunk), "
@@ -836,7 +913,9 @@ def run_ffn(args):
 
     for _ in range(3):
         unfused()
-    unfused_ms = time_loop(unfused, args.steps, stream)
+    rounds, per_round = 4, max(3, args.steps // 4)
+    pair = interleaved({"fused": chain, "unfused": unfused}, rounds, per_round, stream)
+    unfused_ms = pair["unfused"]
     clocks = sampler.stop()
     del G, Hu, P
 
@@ -852,8 +931,10 @@ def run_ffn(args):
         "gpu_launches": 2 * args.steps, "clocks": clocks,
         "stages": {"ag_gemm_ms": ag_ms, "gemm_rs_ms": rs_ms},
         "unfused": {"ms_per_step": unfused_ms, "value": flops / (unfused_ms / 1e3) / 1e12,
-                    "fused_speedup": unfused_ms / ms_step,
-                    "note": "gather copy, bmm, bmm into fp32 partials, separate reduce kernel"},
+                    "fused_ms_interleaved": pair["fused"],
+                    "fused_speedup": unfused_ms / pair["fused"],
+                    "note": "gather copy, bmm, bmm into fp32 partials, separate reduce kernel; "
+                            "fused and unfused timed in interleaved rounds"},
     }
     print(json.dumps(line))
     ag.close()
@@ -874,6 +955,9 @@ def main(argv=None):
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused-only", action="store_true",
+                    help="run only the unfused arm (cuBLAS bmm into fp32 partials + reduce "
+                         "kernel); used for profiling runs")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the fused kernel (no e2e, baselines, ablation or CPU oracle); "
                          "used for profiling runs")
