@@ -613,20 +613,36 @@ def run_ours(args):
     cold_ms = sorted(a.elapsed_time(b) for a, b in zip(cs, ce))
 
     # the library's other reductions: last-arriver (rank-order fold) and the
-    # two-level fold (two rank groups, then their sums)
-    other_mode = {}
+    # two-level fold (two rank groups, then their sums), each timed in
+    # interleaved rounds with the default (every call leaves the tile state
+    # words at 0, so the mode may change between calls)
     mode0 = op.plan["reduce_mode"]
-    for mode, name in ((binding.GEMM_RS_REDUCE_LAST_ARRIVER, "last_arriver"),
-                       (binding.GEMM_RS_REDUCE_CHAIN, "chain"),
-                       (binding.GEMM_RS_REDUCE_TWO_LEVEL, "two_level")):
-        if mode == mode0:
-            continue
-        binding.gemm_rs_set_reduce_mode(op.handle, mode)
-        for _ in range(3):
+
+    def with_mode(m):
+        def run():
+            binding.gemm_rs_set_reduce_mode(op.handle, m)
             step()
-        other_mode[name] = {"ms_per_step": time_loop(step, args.steps, stream),
+        return run
+    modes = {"last_arriver": binding.GEMM_RS_REDUCE_LAST_ARRIVER,
+             "chain": binding.GEMM_RS_REDUCE_CHAIN,
+             "two_level": binding.GEMM_RS_REDUCE_TWO_LEVEL}
+    arms = {"default": with_mode(mode0)}
+    arms.update({name: with_mode(m) for name, m in modes.items() if m != mode0})
+    for fn in arms.values():
+        for _ in range(3):
+            fn()
+    res = interleaved(arms, rounds, per_round, stream)
+    other_mode = {}
+    for name, m in modes.items():
+        if m == mode0:
+            continue
+        binding.gemm_rs_set_reduce_mode(op.handle, m)
+        other_mode[name] = {"ms_per_step": res[name], "default_ms_interleaved": res["default"],
                             "plan": op.plan}
-        binding.gemm_rs_set_reduce_mode(op.handle, mode0)
+    binding.gemm_rs_set_reduce_mode(op.handle, mode0)
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout in the reduce-mode comparison: " +
+                           binding.gemm_rs_last_error())
     clocks = sampler.stop()
 
     # ---- roofline of the fused kernel (the only kernel of the step)

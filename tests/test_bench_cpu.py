@@ -1,0 +1,47 @@
+"""Host-side helpers of bench.py (no GPU): the interleaved timing rounds and the
+keys that tie a committed ncu summary to a kernel source and plan."""
+import bench
+
+
+def test_interleaved_alternates_order_and_averages():
+    calls = []
+
+    def fake_timer(fn, n, stream):
+        calls.append((fn(), n))
+        return {"a": 1.0, "b": 3.0}[calls[-1][0]] + len(calls) * 0.0
+
+    arms = {"a": lambda: "a", "b": lambda: "b"}
+    res = bench.interleaved(arms, 4, 7, None, timer=fake_timer)
+    assert [c[0] for c in calls] == ["a", "b", "b", "a", "a", "b", "b", "a"]
+    assert all(n == 7 for _, n in calls)
+    assert res == {"a": 1.0, "b": 3.0}
+
+
+def test_interleaved_sees_a_drift_equally():
+    """A clock that slows every call by the same step affects both arms alike
+    when the order alternates."""
+    t = [0]
+
+    def drifting(fn, n, stream):
+        t[0] += 1
+        return fn() + 0.1 * t[0]
+
+    res = bench.interleaved({"x": lambda: 1.0, "y": lambda: 1.0}, 4, 1, None, timer=drifting)
+    assert abs(res["x"] - res["y"]) < 1e-12
+
+
+def test_plan_keys():
+    assert bench.plan_key({"bm": 256, "bn": 256, "stages": 7, "grid": 152, "colgroup": 8,
+                           "rowgroup": 2, "rank_order": 1, "reduce_mode": 0}) == \
+        "bm=256 bn=256 colgroup=8 rowgroup=2 rank_order=1 reduce_mode=0"
+    assert bench.plan_key({"grid": 152, "stages": 7, "slice_rows": 8, "slices": 64}) == \
+        "grid=152 stages=7 slice_rows=8 slices=64"
+    assert bench.kernel_name({"bm": 256}) == "gemm_rs_pair_kernel"
+    assert bench.kernel_name({"bm": 128}) == "gemm_rs_fused_kernel"
+
+
+def test_recorded_traffic_needs_a_matching_plan():
+    plan = {"bm": 256, "bn": 256, "stages": 7, "grid": 152, "colgroup": 3, "rowgroup": 2,
+            "rank_order": 1, "reduce_mode": 0}
+    assert bench.recorded_traffic("gemm_rs_pair_kernel", "ffn_w8_m4096", plan) is None
+    assert bench.recorded_traffic("gemm_rs_pair_kernel", "no_such_workload", plan) is None

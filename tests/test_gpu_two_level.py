@@ -98,3 +98,25 @@ def test_one_level_folds_are_rank_order(mode):
                       rank_order=1)
     np.testing.assert_array_equal(
         y, oracle.gemm_rs(bf16_bits(A), bf16_bits(B), None, 1.0, 0.0, "fp32"))
+
+
+@pytest.mark.gpu
+def test_reduce_mode_may_change_between_calls():
+    """Every call leaves the tile state words at 0 in every mode, so one handle
+    may switch modes between calls: each call equals a fresh handle's result in
+    that mode, bit for bit, and the state words end at 0."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 8, 2048, 1536, 64
+    A, B = order_sensitive_inputs(W, M, N, Kpr, seed=11)
+    fresh = {m: run_gpu(A, B, None, W, M, N, Kpr, 1.0, 0.0, "fp32", reduce_mode=m)[0]
+             for m in (0, 1, 2)}
+    dev = torch.device("cuda", 0)
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device=dev)
+    Ad, Bd = A.to(dev), B.to(dev)
+    for m in (2, 0, 1, 2, 1, 0, 2):
+        b.gemm_rs_set_reduce_mode(op.handle, m)
+        Y = op.run(Ad, Bd)
+        torch.cuda.synchronize()
+        assert op.status() == 0
+        np.testing.assert_array_equal(Y.cpu().numpy(), fresh[m])
+        assert int(op.flags_view().abs().sum()) == 0
