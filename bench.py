@@ -239,6 +239,27 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def host_cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: implementer
+    and part numbers), else the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = (x.strip() for x in line.split(":", 1))
+                    fields.setdefault(k, v)
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if fields.get("CPU implementer"):
+        return (f"{platform.machine()} implementer {fields['CPU implementer']} "
+                f"part {fields.get('CPU part', '?')}")
+    return platform.machine() or "unknown"
+
+
 def calibrate_rows(w, A, B, C, threads: int, target_s: float):
     """Rows per oracle sample such that one sample takes about target_s seconds."""
     t, n = oracle_sample(w, A, B, C, threads, threads)
@@ -274,7 +295,8 @@ def run_reference(args):
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                         "cpu": host_cpu_model(), "kind": "oracle",
                          "sample": f"{rows} of {w.M} output rows per step (all N columns, all W ranks)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -672,6 +694,7 @@ def run_ours(args):
         rows, _ = calibrate_rows(w, A, B, C, cores, target_s=args.cpu_seconds)
         sec, n = oracle_sample(w, A, B, C, rows, cores)
         cpu = {"value": 2.0 * n * w.N * w.K / sec / 1e12, "unit": "TFLOP/s", "cores": cores,
+               "cpu": host_cpu_model(),
                "kind": "oracle", "seconds": sec,
                "sample": f"{n} of {w.M} output rows (all N columns, all W ranks), evenly spaced"}
 
@@ -829,7 +852,7 @@ def run_ag(args):
         oracle.ag_gemm(bf16_bits(X), bf16_bits(B1), w.alpha, w.y_dtype, rows=rows, threads=cores)
         sec = time.perf_counter() - t
         cpu = {"value": 2.0 * len(rows) * w.W * w.N * w.K / sec / 1e12, "unit": "TFLOP/s",
-               "cores": cores, "kind": "oracle", "seconds": sec,
+               "cores": cores, "cpu": host_cpu_model(), "kind": "oracle", "seconds": sec,
                "sample": f"{len(rows)} of {w.M} rows of every rank's output, evenly spaced"}
 
     achieved = w.flops / (kernel_avg / 1e3) / 1e12
