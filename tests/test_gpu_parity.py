@@ -182,15 +182,18 @@ def test_device_schedule_record_matches_schedule_and_oracle():
         np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("tile", [(128, 256), (256, 256)])
-def test_timeout_path_reports_and_recovers(tile):
+def test_timeout_path_reports_and_recovers(tile, mode):
     """A stalled producer makes the MMA warp's bounded wait run out.  The
-    kernel records the timeout, exits, and the context stays usable."""
+    kernel records the timeout, exits, and the context stays usable, in every
+    reduce mode."""
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
-    W, M, N, Kpr = 2, 512, 256, 128
+    W, M, N, Kpr = 4, 512, 256, 128
     A, B, _ = inputs(W, M, N, Kpr, "int")
     op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0", tile_m=tile[0],
                   tile_n=tile[1])
+    b.gemm_rs_set_reduce_mode(op.handle, mode)
     Ad, Bd = A.cuda(), B.cuda()
     b.gemm_rs_set_timeout_cycles(op.handle, 1 << 22)
     b.gemm_rs_set_debug(op.handle, 0, b.GEMM_RS_DEBUG_STALL_PRODUCER)
