@@ -80,7 +80,10 @@ enum {
     GEMM_RS_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (message has the detail) */
     GEMM_RS_ERR_TIMEOUT = -5,     /* a device-side wait ran past its cycle limit */
     GEMM_RS_ERR_UNSUPPORTED = -6, /* dtype combination or device (needs sm_103) not supported */
-    GEMM_RS_ERR_WORKSPACE = -7    /* workspace smaller than gemm_rs_workspace_bytes() */
+    GEMM_RS_ERR_WORKSPACE = -7,   /* workspace smaller than gemm_rs_workspace_bytes() */
+    GEMM_RS_ERR_BOUNDS = -8       /* checked build only (libgemm_rs_checked.so, compiled with
+                                     GEMM_RS_CHECKED): an access of the epilogue or a fold
+                                     outside its buffer was caught and skipped */
 };
 
 /* How the W partials of an output tile are reduced (gemm_rs_set_reduce_mode). */
@@ -189,7 +192,8 @@ GEMM_RS_API const char *gemm_rs_last_error(void);
  * word.  Returns GEMM_RS_OK, or GEMM_RS_ERR_TIMEOUT if a kernel of this
  * handle gave up on a wait since the last check.  After a timeout, Y of that
  * run is incomplete and the tile counters may be non-zero: call
- * gemm_rs_reset before the next run.
+ * gemm_rs_reset before the next run.  The checked build can also return
+ * GEMM_RS_ERR_BOUNDS (see the error codes).
  */
 GEMM_RS_API int gemm_rs_status(gemm_rs_t h, gemm_rs_stream_t stream);
 

@@ -19,7 +19,9 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgemm_rs.so")
+# GEMM_RS_LIBRARY selects another build of this library (the tests load the
+# checked build, libgemm_rs_checked.so, that way, in a process of their own).
+LIB_PATH = os.environ.get("GEMM_RS_LIBRARY") or os.path.join(_HERE, "libgemm_rs.so")
 
 GEMM_RS_BF16 = 0
 GEMM_RS_FP32 = 1
@@ -32,6 +34,7 @@ GEMM_RS_ERR_CUDA = -4
 GEMM_RS_ERR_TIMEOUT = -5
 GEMM_RS_ERR_UNSUPPORTED = -6
 GEMM_RS_ERR_WORKSPACE = -7
+GEMM_RS_ERR_BOUNDS = -8
 
 GEMM_RS_DEBUG_STALL_PRODUCER = 1
 

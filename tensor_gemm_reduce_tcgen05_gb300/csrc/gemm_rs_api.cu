@@ -330,7 +330,11 @@ int colgroup_of(const gemm_rs_s *h)
 
 extern "C" {
 
+#ifdef GEMM_RS_CHECKED
+const char *gemm_rs_version(void) { return "gemm_rs 0.1 (sm_103a, tcgen05, checked)"; }
+#else
 const char *gemm_rs_version(void) { return "gemm_rs 0.1 (sm_103a, tcgen05)"; }
+#endif
 
 const char *gemm_rs_last_error(void) { return g_err.c_str(); }
 
@@ -599,6 +603,8 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.y_fp32 = h->y_dtype == GEMM_RS_FP32 ? 1 : 0;
     a.part = reinterpret_cast<float *>(h->ws + h->L.part_off);
     a.flags = reinterpret_cast<uint32_t *>(h->ws + h->L.flags_off);
+    a.part_floats = static_cast<int64_t>(h->L.part_bytes / sizeof(float));
+    a.nflags = static_cast<int64_t>(h->L.flags_bytes / sizeof(uint32_t));
     a.status = reinterpret_cast<uint32_t *>(h->ws);
     a.record = h->record;
     a.timeout = h->timeout;
@@ -652,6 +658,9 @@ int gemm_rs_status(gemm_rs_t h, gemm_rs_stream_t stream)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(e, "clearing the status word");
+    if (word == gemm_rs::kStatusOutOfBounds)
+        return fail(GEMM_RS_ERR_BOUNDS,
+                    "checked build: an access outside its buffer was caught and skipped");
     static const char *role[] = {"?", "TMA producer", "MMA issuer", "epilogue", "reducer"};
     return fail(GEMM_RS_ERR_TIMEOUT, "device wait timed out in the %s (status %u)",
                 role[word < 5 ? word : 0], word);
@@ -867,6 +876,8 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.y_fp32 = y_dtype == GEMM_RS_FP32 ? 1 : 0;
     a.part = reinterpret_cast<float *>(scratch + L.part_off);
     a.flags = reinterpret_cast<uint32_t *>(scratch + L.flags_off);
+    a.part_floats = static_cast<int64_t>(L.part_bytes / sizeof(float));
+    a.nflags = static_cast<int64_t>(L.flags_bytes / sizeof(uint32_t));
     a.status = reinterpret_cast<uint32_t *>(scratch);
     a.record = nullptr;
     a.timeout = 1ull << 32;

@@ -73,6 +73,7 @@ enum : uint32_t {
     kStatusTimeoutMma = 2,
     kStatusTimeoutEpilogue = 3,
     kStatusTimeoutReducer = 4,
+    kStatusOutOfBounds = 5, // checked build: an access outside its buffer was skipped
 };
 
 template <int BN>
@@ -117,6 +118,8 @@ struct KernelArgs {
     long long chain_wait; // SM cycles a chain position waits for its turn before storing
     int split;      // chain mode, two-level fold: ranks [0, split) and [split, W) fold
                     // separately, then the two sums are added (0: one fold over all W)
+    int64_t part_floats; // floats in the partial slots, and state words: the buffers'
+    int64_t nflags;      // extents, for the checked build's bounds checks
     int64_t R;      // rows per chunk
     int64_t total;  // W * nM * nN work items
     float alpha, beta;
@@ -162,6 +165,48 @@ constexpr int smem_bytes_pair()
     return 1024 + PairCfg<BN>::kStages * PairCfg<BN>::kStageBytes + int(sizeof(SmemCtl));
 }
 static_assert(smem_bytes_pair<256>() <= 232448, "the pair kernel's shared memory exceeds 227 KB");
+
+// Checked build (compiled with GEMM_RS_CHECKED): the global accesses of the
+// epilogue and the folds are tested against their buffers first.  An access
+// outside its buffer is skipped, and the first one is recorded in the status
+// word.  In the normal build every check is the constant true.
+__device__ __forceinline__ bool bounds_ok(const KernelArgs &a, bool ok)
+{
+#ifdef GEMM_RS_CHECKED
+    if (!ok)
+        atomicCAS(a.status, 0u, static_cast<uint32_t>(kStatusOutOfBounds));
+    return ok;
+#else
+    (void)a;
+    (void)ok;
+    return true;
+#endif
+}
+
+// [p, p + n) lies in the partial slots.
+__device__ __forceinline__ bool in_part(const KernelArgs &a, const float *p, int64_t n)
+{
+#ifdef GEMM_RS_CHECKED
+    const int64_t off = p - a.part;
+    return bounds_ok(a, off >= 0 && off + n <= a.part_floats);
+#else
+    (void)p;
+    (void)n;
+    return bounds_ok(a, true);
+#endif
+}
+
+// Columns [n, n + 8) of row m lie in Y and C ([M][N]).
+__device__ __forceinline__ bool in_mn(const KernelArgs &a, int64_t m, int64_t n)
+{
+    return bounds_ok(a, m >= 0 && m < a.M && n >= 0 && n + 8 <= a.N);
+}
+
+// A state word lies in the flags.
+__device__ __forceinline__ bool in_flags(const KernelArgs &a, const uint32_t *f)
+{
+    return bounds_ok(a, f >= a.flags && f - a.flags < a.nflags);
+}
 
 __device__ __forceinline__ void report(const KernelArgs &a, SmemCtl *ctl, uint32_t code)
 {
@@ -316,6 +361,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ void store_y8(const KernelArgs &a, int64_t m, int64_t n, float4 lo,
                                          float4 hi)
 {
+#ifdef GEMM_RS_CHECKED
+    if (!in_mn(a, m, n))
+        return;
+#endif
     if (a.y_fp32) {
         float *yp = static_cast<float *>(a.Y) + m * a.N + n;
         ptx::st_f4(yp, lo);
@@ -382,22 +431,29 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
         // loaded at once.  Fixed order: y = slot[0], then y = y + slot[s].
         const float *sb = qb + slab * 1024 + lane * 4;
         const float *s0 = q0 + slab * 1024 + lane * 4;
+        // a lane touches floats [p, p + 7*128 + 4) of a slot's slab block
+        constexpr int64_t kLaneSpan = 7 * 128 + 4;
+        const bool sb_ok = in_part(a, sb, kLaneSpan);
         float4 y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            y[j] = ptx::ld_cg_f4(sb + j * 128);
+            y[j] = sb_ok ? ptx::ld_cg_f4(sb + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
         // Two slots per round trip (16 loads in flight), added in slot order.
 #pragma unroll 1
         for (int sl = first; sl <= hi; sl += 2) {
             const bool two = sl + 1 <= hi;
+            const float *pu = s0 + static_cast<int64_t>(sl) * Cfg::kSlotFloats;
+            const float *pw = pu + Cfg::kSlotFloats;
+            const bool u_ok = in_part(a, pu, kLaneSpan);
+            const bool w_ok = !two || in_part(a, pw, kLaneSpan);
             float4 u[8], w2[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                u[j] = ptx::ld_cg_f4(s0 + static_cast<int64_t>(sl) * Cfg::kSlotFloats + j * 128);
+                u[j] = u_ok ? ptx::ld_cg_f4(pu + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
             if (two) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    w2[j] = ptx::ld_cg_f4(s0 + static_cast<int64_t>(sl + 1) * Cfg::kSlotFloats + j * 128);
+                    w2[j] = w_ok ? ptx::ld_cg_f4(pw + j * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -418,7 +474,7 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
                 if (row_ok && n < a.N) // N is a multiple of 8
                     store_y8(a, m, n, y[2 * j2], y[2 * j2 + 1]);
             }
-        } else {
+        } else if (sb_ok) {
             float *dst = qb + slab * 1024 + lane * 4;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -427,11 +483,13 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
         // Every lane has read this slab of every slot: drop the dead lines
         // (lane l drops line l of each 4 KB block).
         __syncwarp();
-        if (to_y)
+        if (to_y && in_part(a, qb + slab * 1024 + lane * 32, 32))
             ptx::discard_l2_line(qb + slab * 1024 + lane * 32);
-        for (int s = first; s <= hi; ++s)
-            ptx::discard_l2_line(q0 + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 +
-                                 lane * 32);
+        for (int s = first; s <= hi; ++s) {
+            float *line = q0 + static_cast<int64_t>(s) * Cfg::kSlotFloats + slab * 1024 + lane * 32;
+            if (in_part(a, line, 32))
+                ptx::discard_l2_line(line);
+        }
     }
 }
 
@@ -541,6 +599,8 @@ __device__ __forceinline__ bool chain_wait_own(uint32_t *flag, uint32_t i, long 
 __device__ __forceinline__ int group_done(const KernelArgs &a, int tile)
 {
     uint32_t *done = a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile;
+    if (!in_flags(a, done))
+        done = a.flags;
     if (ptx::atom_add_acq_rel_gpu(done, 1u) == 0u)
         return 0;
     ptx::st_relaxed_gpu(done, 0u);
@@ -636,6 +696,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         const int cpos = a.split > 0 ? r - base : pos;
         const int clen = a.split > 0 ? (grp ? a.W - a.split : a.split) : a.W;
         uint32_t *cflag = a.flags + static_cast<int64_t>(grp) * a.nM * a.nN + tile;
+        if (!in_flags(a, cflag))
+            cflag = a.flags; // checked build only: keep the atomics in bounds
         // Chain mode: try to take the fold while the accumulator is still being
         // computed, so the decision is ready when it lands.
         if (etid == 0)
@@ -659,6 +721,7 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             // already done, this position adds all three terms and writes Y
             // (direct = 2) instead of publishing its group's sum.
             if (a.split > 0 && ctl->epi_direct[buf] != 0 && cpos == clen - 1 &&
+                in_flags(a, a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile) &&
                 ptx::ld_acquire_gpu(a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile) != 0u)
                 ctl->epi_direct[buf] = 2;
         }
@@ -719,9 +782,11 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         for (int slab = sl0; slab < (q_live ? sl1 : sl0); ++slab) {
             float4 rs[8];
             if (add_prev) {
+                const bool ok = in_part(a, prev + slab * 1024, 7 * 128 + 4);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    rs[j] = ptx::ld_cg_f4(prev + slab * 1024 + j * 128);
+                    rs[j] = ok ? ptx::ld_cg_f4(prev + slab * 1024 + j * 128)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             uint32_t v[32];
             if (a.nK > 0) {
@@ -753,7 +818,7 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
 #pragma unroll
                 for (int g8 = 0; g8 < 4; ++g8) {
                     const int64_t n = n0 + 8 * g8;
-                    if (row_ok && n < a.N) {
+                    if (row_ok && n < a.N && in_mn(a, m, n)) {
                         const uint4 c = ptx::ld_nc_u4(a.C + m * a.N + n);
                         const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -778,9 +843,11 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             if (final) {
                 // then the other group's sum (fp32 addition is commutative, so
                 // this is y0 + y1 whichever group finishes second)
+                const bool ok = in_part(a, other + slab * 1024, 7 * 128 + 4);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    rs[j] = ptx::ld_cg_f4(other + slab * 1024 + j * 128);
+                    rs[j] = ok ? ptx::ld_cg_f4(other + slab * 1024 + j * 128)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     p[4 * j] = rs[j].x + p[4 * j];
@@ -802,11 +869,13 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             } else if (add_l2) {
                 // running sum + this position's partial, added in L2
                 float *dst = slot + slab * 1024;
+                if (in_part(a, dst, 7 * 128 + 4)) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    ptx::red_add_f4(dst + j * 128,
-                                    make_float4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
-            } else {
+                    for (int j = 0; j < 8; ++j)
+                        ptx::red_add_f4(dst + j * 128, make_float4(p[4 * j], p[4 * j + 1],
+                                                                   p[4 * j + 2], p[4 * j + 3]));
+                }
+            } else if (in_part(a, slot + slab * 1024, 7 * 128 + 4)) {
                 float *dst = slot + slab * 1024;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
@@ -817,10 +886,12 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
             if (add_prev || final) {
                 // the sums read are dead: drop their lines of this warp's 4 KB block
                 __syncwarp();
-                if (add_prev)
-                    ptx::discard_l2_line(prev - lane * 4 + slab * 1024 + lane * 32); // line `lane`
-                if (final)
-                    ptx::discard_l2_line(other - lane * 4 + slab * 1024 + lane * 32);
+                const float *lp = prev - lane * 4 + slab * 1024 + lane * 32; // line `lane`
+                const float *lo = other - lane * 4 + slab * 1024 + lane * 32;
+                if (add_prev && in_part(a, lp, 32))
+                    ptx::discard_l2_line(lp);
+                if (final && in_part(a, lo, 32))
+                    ptx::discard_l2_line(lo);
             }
         }
 
@@ -832,6 +903,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
         if (etid == 0) {
             if (!a.chain) {
                 uint32_t *flag = a.flags + tile;
+                if (!in_flags(a, flag))
+                    flag = a.flags;
                 const uint32_t old = ptx::atom_add_acq_rel_gpu(flag, 1u);
                 if (old == static_cast<uint32_t>(a.W - 1)) {
                     // Last arriver: the counter goes back to 0 for the next call
@@ -847,7 +920,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                 if (direct) {
                     if (cpos == clen - 1) {
                         ptx::st_relaxed_gpu(cflag, 0u); // back to 0 for the next call
-                        if (final) // Y is written; the group count goes back to 0
+                        if (final && in_flags(a, a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile))
+                            // Y is written; the group count goes back to 0
                             ptx::st_relaxed_gpu(a.flags + 2 * static_cast<int64_t>(a.nM) * a.nN + tile, 0u);
                         else if (a.split > 0)
                             combine = group_done(a, tile);

@@ -1,0 +1,85 @@
+"""The bounds-checked build (libgemm_rs_checked.so, compiled with
+GEMM_RS_CHECKED) runs the parity cases in a process of its own: every global
+access of the epilogue and the folds is tested against its buffer, and one
+outside it would be skipped and reported as GEMM_RS_ERR_BOUNDS.  The runs must
+report none and stay bit-exact.  (A memory checker is not available on this
+pool; this and the NaN-poison tests stand in for it.)
+
+Also fault injection on the host side of the state words: a workspace whose
+tile state words hold garbage gives a wrong result but no hang and no fault
+(every wait is bounded and every slot index comes from the schedule), and
+gemm_rs_reset restores exact results."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import inputs, oracle_y, run_gpu, to_np_y
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CHECKED = os.path.join(ROOT, "tensor_gemm_reduce_tcgen05_gb300", "libgemm_rs_checked.so")
+
+SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np
+from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+from helpers import inputs, oracle_y, run_gpu
+assert "checked" in b.gemm_rs_version(), b.gemm_rs_version()
+cases = 0
+shapes = [(2, 256, 256, 256), (3, 300, 520, 200), (8, 64, 512, 192), (1, 200, 72, 64),
+          (16, 16 * 9, 136, 72), (4, 512, 768, 128)]
+for (W, M, N, Kpr) in shapes:
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
+    ref = oracle_y(A, B, C, 0.5, 1.0, "fp32")
+    for tile in ((128, 256), (128, 128), (128, 64), (256, 256)):
+        for mode in (0, 1, 2):
+            for order in (1, 2):
+                y, plan, op = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, "fp32", tile_m=tile[0],
+                                      tile_n=tile[1], reduce_mode=mode, rank_order=order,
+                                      poison=True, calls=2)
+                np.testing.assert_array_equal(y, ref)
+                cases += 1
+print("checked cases", cases)
+"""
+
+
+def test_checked_build_finds_no_access_out_of_bounds():
+    assert os.path.exists(CHECKED), "build() makes the checked library too"
+    env = dict(os.environ, GEMM_RS_LIBRARY=CHECKED)
+    r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT, tests=HERE)], env=env,
+                       capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "checked cases 144" in r.stdout
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_garbage_state_words_then_reset(mode):
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 4, 512, 768, 128
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    dev = torch.device("cuda", 0)
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device=dev)
+    b.gemm_rs_set_reduce_mode(op.handle, mode)
+    b.gemm_rs_set_timeout_cycles(op.handle, 1 << 26)
+    Ad, Bd = A.to(dev), B.to(dev)
+    flags = op.flags_view()
+    g = torch.Generator(device="cpu").manual_seed(mode)
+    flags.copy_(torch.randint(0, 1 << 30, flags.shape, generator=g, dtype=torch.int32))
+    op.run(Ad, Bd)
+    torch.cuda.synchronize()
+    assert op.status() in (b.GEMM_RS_OK, b.GEMM_RS_ERR_TIMEOUT)
+    op.reset()
+    b.gemm_rs_set_timeout_cycles(op.handle, 1 << 32)
+    for _ in range(2):
+        Y = op.run(Ad, Bd)
+        torch.cuda.synchronize()
+        assert op.status() == b.GEMM_RS_OK
+        np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+        assert int(op.flags_view().abs().sum()) == 0
