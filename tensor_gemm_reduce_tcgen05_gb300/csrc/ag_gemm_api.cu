@@ -287,6 +287,9 @@ int ag_gemm_status(ag_gemm_t h, gemm_rs_stream_t stream)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(e, "clearing the status word");
+    if (word == gemm_rs::kStatusOutOfBounds)
+        return fail(GEMM_RS_ERR_BOUNDS,
+                    "checked build: an access outside its buffer was caught and skipped");
     return fail(GEMM_RS_ERR_TIMEOUT, "device wait timed out in the AG+GEMM kernel (status %u)", word);
 }
 

@@ -85,6 +85,22 @@ __host__ __device__ __forceinline__ void ag_decode(const AgArgs &g, int64_t e, i
 
 // Bounded wait for a chunk signal: true once *p has reached `target` (compared
 // modulo 2^32), false when `limit` cycles pass or the CTA aborts.
+// Checked build (GEMM_RS_CHECKED): as in the GEMM+RS kernel, an access outside
+// its buffer is skipped and recorded in the status word; the normal build
+// compiles the checks away.
+__device__ __forceinline__ bool ag_bounds_ok(const AgArgs &g, bool ok)
+{
+#ifdef GEMM_RS_CHECKED
+    if (!ok)
+        atomicCAS(g.status, 0u, static_cast<uint32_t>(kStatusOutOfBounds));
+    return ok;
+#else
+    (void)g;
+    (void)ok;
+    return true;
+#endif
+}
+
 __device__ __forceinline__ bool wait_signal(const uint32_t *p, uint32_t target, unsigned long long limit,
                                             const volatile int *abort_flag)
 {
@@ -125,7 +141,7 @@ __device__ __forceinline__ void run_ag_producer(const AgArgs &g, const KernelArg
             rec[3] = static_cast<int32_t>(cid);
         }
         const bool local = c == r;
-        if (!local) {
+        if (!local && ag_bounds_ok(g, r >= 0 && r < g.W && c >= 0 && c < g.W)) {
             if (!wait_signal(g.ready + r * g.W + c, target, g.timeout, abort_flag)) {
                 ok = false;
                 break;
@@ -245,6 +261,8 @@ __device__ __forceinline__ void run_ag_epilogue(const AgArgs &g, const KernelArg
                 const int64_t n = n0 + 8 * g8;
                 if (!row_ok || n >= g.N) // N is a multiple of 8
                     continue;
+                if (!ag_bounds_ok(g, r >= 0 && r < g.W && m >= 0 && m < g.M && n + 8 <= g.N))
+                    continue;
                 float p[8];
 #pragma unroll
                 for (int e2 = 0; e2 < 8; ++e2)
@@ -289,7 +307,10 @@ __device__ __forceinline__ void run_ag_copy(const AgArgs &g, int ct)
         const int64_t row0 = static_cast<int64_t>(c) * g.R + static_cast<int64_t>(j) * g.slice_rows;
         const uint4 *src = reinterpret_cast<const uint4 *>(g.X + row0 * g.K);
         uint4 *dst = reinterpret_cast<uint4 *>(g.G + (static_cast<int64_t>(r) * g.M + row0) * g.K);
-        int64_t i = ct;
+        // the slice's rows [row0, row0 + slice_rows) of X and of rank r's buffer
+        const bool in = ag_bounds_ok(g, row0 >= 0 && row0 + g.slice_rows <= g.M && r < g.W &&
+                                            c >= 0 && c < g.W);
+        int64_t i = in ? ct : n16;
         for (; i + 3 * 128 < n16; i += 4 * 128) {
             uint4 t[4];
 #pragma unroll
@@ -303,7 +324,7 @@ __device__ __forceinline__ void run_ag_copy(const AgArgs &g, int ct)
             ptx::st_u4(dst + i, ptx::ld_nc_u4(src + i));
         // Every copy thread's stores are ordered before the signal's release.
         ptx::named_bar_sync(kBarCopy, 128);
-        if (ct == 0)
+        if (ct == 0 && in)
             ptx::atom_add_acq_rel_gpu(g.ready + r * g.W + c, 1u);
     }
 }

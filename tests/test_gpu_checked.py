@@ -1,7 +1,8 @@
 """The bounds-checked build (libgemm_rs_checked.so, compiled with
 GEMM_RS_CHECKED) runs the parity cases in a process of its own: every global
-access of the epilogue and the folds is tested against its buffer, and one
-outside it would be skipped and reported as GEMM_RS_ERR_BOUNDS.  The runs must
+access of the GEMM+RS epilogue and folds, and of the AG+GEMM copies, signals
+and H stores, is tested against its buffer, and one outside it would be
+skipped and reported as GEMM_RS_ERR_BOUNDS.  The runs must
 report none and stay bit-exact.  (A memory checker is not available on this
 pool; this and the NaN-poison tests stand in for it.)
 
@@ -47,6 +48,26 @@ for (W, M, N, Kpr) in shapes:
                 np.testing.assert_array_equal(y, ref)
                 cases += 1
 print("checked cases", cases)
+from tensor_gemm_reduce_tcgen05_gb300.inputs import make_ag_inputs
+from helpers import to_np_y
+import oracle, torch
+ag_cases = 0
+for (W, M, N, K) in [(2, 512, 256, 256), (3, 768, 264, 200), (1, 256, 72, 64),
+                     (8, 2048, 512, 128), (16, 16 * 256, 64, 64), (4, 2048, 1000, 136)]:
+    X, B1 = make_ag_inputs(W, M, N, K, "int", "int")
+    for y_dtype in ("fp32", "bf16"):
+        op = b.AgGemm(M, N, K, W, 1.0, y_dtype, device="cuda:0")
+        H = op.new_output()
+        H.view(torch.uint8).fill_(0xFF)
+        for _ in range(2):
+            op.run(X.cuda(), B1.cuda(), H)
+        torch.cuda.synchronize()
+        assert op.status() == 0
+        np.testing.assert_array_equal(to_np_y(H), oracle.ag_gemm(
+            oracle.bf16_from_float(X.float().numpy()), oracle.bf16_from_float(B1.float().numpy()),
+            1.0, y_dtype))
+        ag_cases += 1
+print("checked ag cases", ag_cases)
 """
 
 
@@ -57,6 +78,7 @@ def test_checked_build_finds_no_access_out_of_bounds():
                        capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     assert "checked cases 144" in r.stdout
+    assert "checked ag cases 12" in r.stdout
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
