@@ -69,7 +69,8 @@ GEMM_RS_API int ag_gemm_run(ag_gemm_t h, const void *X, const void *B1, void *H,
                             gemm_rs_stream_t stream);
 
 /* Synchronise `stream`, then read and clear the status word: GEMM_RS_OK or
- * GEMM_RS_ERR_TIMEOUT.  After a timeout call ag_gemm_reset. */
+ * GEMM_RS_ERR_TIMEOUT (or, in the checked build, GEMM_RS_ERR_BOUNDS).  After
+ * a timeout call ag_gemm_reset. */
 GEMM_RS_API int ag_gemm_status(ag_gemm_t h, gemm_rs_stream_t stream);
 
 /* Zero the status word and the chunk signals (one memset on `stream`). */

@@ -18,17 +18,21 @@
  *     beta*C + EVT_Compute0).  So beta*C is added once per rank: the result
  *     is alpha * sum_r(A_r B_r) + W * beta * C.  C is never read when
  *     beta == 0.
- *   - The partials are fp32.  They are summed in fixed rank order
- *     ((p_0 + p_1) + p_2) + ... in fp32, so results are bit-identical from
- *     run to run.  A bf16 Y is rounded to nearest even.
+ *   - The partials are fp32 and are summed in fp32 in a fixed order, so
+ *     results are bit-identical from run to run: rank order
+ *     ((p_0 + p_1) + p_2) + ... by default (see GEMM_RS_REDUCE_* for the
+ *     orders of the other modes).  A bf16 Y is rounded to nearest even.
  *
- *   One call runs one fused kernel.  Each output tile's partial goes into a
- *   workspace slot keyed to its chunk.  A 32-bit arrival counter per output
- *   tile finds the last rank to arrive ("flux实现：sm80 gemm+rs", section
- *   "evt_store_d()": a globally unique id per tile and a barrier flag per
- *   tile; "flux精读" §4.2: signals are 32-bit contiguous memory that lives as
- *   long as the op).  That rank's CTA reduces the tile and resets the counter
- *   to zero.  So no memset, separate reduce kernel or host sync runs between
+ *   One call runs one fused kernel.  Each output tile's partials meet in
+ *   workspace slots keyed to the tile's chunk, coordinated by 32-bit state
+ *   words per output tile ("flux实现：sm80 gemm+rs", section "evt_store_d()": a
+ *   globally unique id per tile and a barrier flag per tile; "flux精读" §4.2:
+ *   signals are 32-bit contiguous memory that lives as long as the op).  In
+ *   the pages' design (GEMM_RS_REDUCE_LAST_ARRIVER) every rank stores its
+ *   partial and the last rank to arrive reduces the tile; by default
+ *   (GEMM_RS_REDUCE_CHAIN) each rank adds its partial onto a running sum as it
+ *   lands and the last one writes Y.  Either way the tile's state words end
+ *   at zero, so no memset, separate reduce kernel or host sync runs between
  *   calls (the page's reduce buffer had to start zeroed and its clear cost tens
  *   of microseconds: "flux实现：sm80 gemm+rs", section "自己的类flux实现").
  *
