@@ -108,13 +108,42 @@ KERNEL_SOURCES = ("gemm_rs_kernel.cuh", "ptx.cuh", "schedule.cuh")
 AG_KERNEL_SOURCES = ("ag_gemm_kernel.cuh", "gemm_rs_kernel.cuh", "ptx.cuh")
 
 
+def code_only(text: str) -> str:
+    """C/C++ source with its comments removed and each line's whitespace
+    trimmed (blank lines dropped): what the compiler sees of the code, so that
+    editing a comment does not change a kernel's identity.  String and
+    character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.strip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+    """Identity of the kernels' code (comments and layout whitespace ignored)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_gemm_reduce_tcgen05_gb300", "csrc")
     for name in sources:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,45 +1,56 @@
-// The fused GEMM + reduce-scatter kernel for sm_103a.
+// The fused GEMM + reduce-scatter kernels for sm_103a.
 //
-// One persistent CTA per SM walks the global tile order of schedule.cuh.
-// Each work item is one rank-tile (r, mt, nt): the 128 x BN output tile
-// (mt, nt) of logical rank r's GEMM A_r * B_r over its K/W shard.
+// Persistent CTAs walk the global tile order of schedule.cuh.  Each work item
+// is one rank-tile (r, mt, nt): an output tile of logical rank r's GEMM
+// A_r * B_r over its K/W shard.  Two kernels share the roles below:
+//   gemm_rs_fused_kernel<BN>   one CTA per 128 x BN tile, tcgen05.mma with
+//                              M = 128 (cta_group::1); one CTA per SM.
+//   gemm_rs_pair_kernel<256>   a cluster of two CTAs per 256 x 256 tile,
+//                              tcgen05.mma with M = 256 (cta_group::2); each
+//                              CTA loads its own 128 rows of A and 128 columns
+//                              of B (no multicast) and drains its own half.
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer (one thread).  For each k-block, it loads the
-//               A_r box [128 x 64] and the B_r boxes [64 x 64] (BN/64 of
-//               them) into a stage of the shared-memory ring, 128-byte
-//               swizzled, and completes the stage's `full` mbarrier.
+//   warp 0      TMA producer (one thread).  For each k-block it loads the A_r
+//               box [128 x 64] and the B_r boxes [64 x 64] into a stage of the
+//               shared-memory ring, 128-byte swizzled, completing the stage's
+//               `full` mbarrier.
 //   warp 1      TMEM allocator and MMA issuer (one thread).  It issues
-//               tcgen05.mma (M = 128, N = BN, K = 16, bf16 -> fp32) into one of
-//               two TMEM accumulators of BN columns each.  tcgen05.commit
-//               frees each stage, and at the end of the tile signals
-//               `acc_full`.
-//   warps 2-5   epilogue visitor.  Each warp drains 32 TMEM lanes (one row
-//               per thread), computes p = alpha*acc + beta*C
-//               ("flux实现：sm80 gemm+rs", section "custom_evt_d()"), and
-//               stores p with 16-byte coalesced stores into the tile's
-//               rank-r slot of the chunk workspace ("evt_store_d()": the
-//               store goes to the reduce-scatter buffer, not to Y).  It then
-//               increments the tile's 32-bit arrival counter.  The rank that
-//               arrives last resets the counter to 0 and queues the tile for
-//               the reducers.
-//   warps 6-9   reducers.  For each queued tile they fold the W partials in
-//               rank order in fp32, convert, and write Y.  They run beside
-//               the epilogue, so a reduction never holds a TMEM accumulator.
-//               In the chain mode (see run_epilogue) there are no queued
-//               tiles, and warps 6-9 are a second epilogue group instead:
-//               each of the eight warps drains half of its lane quarter's
-//               column slabs.
+//               tcgen05.mma (bf16 -> fp32) into one of two TMEM accumulators;
+//               tcgen05.commit frees each stage and, at the end of the tile,
+//               signals `acc_full`.
+//   warps 2-5   epilogue visitor.  Each warp drains 32 TMEM lanes (one row per
+//               thread) and computes p = alpha*acc + beta*C
+//               ("flux实现：sm80 gemm+rs", section "custom_evt_d()").  Where p
+//               goes is the reduce mode's (run_epilogue):
+//                 LAST_ARRIVER  p is stored in the tile's rank-r slot of the
+//                               chunk workspace ("evt_store_d()": the store
+//                               goes to the reduce-scatter buffer, not to Y);
+//                               the rank that arrives last on the tile's
+//                               32-bit counter resets it and queues the tile.
+//                 CHAIN         p is added onto the tile's running sum when
+//                               its turn comes (or stored, and folded on by
+//                               whoever holds the fold); the last position
+//                               writes Y.
+//                 TWO_LEVEL     CHAIN within each of two rank groups; the
+//                               group that finishes second adds the two sums.
+//   warps 6-9   LAST_ARRIVER: reducers, folding each queued tile's W partials
+//               in rank order and writing Y beside the epilogue (a reduction
+//               never holds a TMEM accumulator).  CHAIN and TWO_LEVEL: a second
+//               epilogue group (each of the eight warps drains half of its lane
+//               quarter's column slabs).
 //
-// There are no waits between CTAs.  The last arriver never waits for
-// anyone, so the kernel cannot deadlock however many CTAs it has (the
-// deadlock of a device-wide barrier with more CTAs than fit at once is
-// described in "flux实现：sm80 gemm+rs", section "device side barrier").
-// Every mbarrier wait is bounded in SM cycles.  A wait that runs out records
-// a code in the status word, and the CTA then drains its TMA loads and MMAs
-// and exits.
+// Waits between CTAs: LAST_ARRIVER has none (the last arriver waits for no one,
+// so the kernel cannot deadlock however many CTAs it has; the deadlock of a
+// device-wide barrier with more CTAs than fit at once is described in
+// "flux实现：sm80 gemm+rs", section "device side barrier").  CHAIN has one,
+// bounded: a position may wait a few thousand cycles for the position before
+// it, which lies earlier in the tile order, so the waits form no cycle.
+// Every mbarrier wait is bounded in SM cycles too.  A wait that runs out
+// records a code in the status word, and the CTA drains its TMA loads and
+// MMAs, frees TMEM and exits.
 //
-// Partial slot layout: slot (tile, r) holds 4 x (BN/32) blocks of 32 rows x 32
+// Partial slot layout: slot (tile, s) holds 4 x (BN/32) blocks of 32 rows x 32
 // columns (fp32).  Inside a block, float4 j (columns 4j .. 4j+3) of row t is
 // at float4 index j*32 + t, so each warp-wide 16-byte store or load covers 512
 // contiguous bytes.  Slots are ordered by row tile, so the slots of the tiles

@@ -45,3 +45,13 @@ def test_recorded_traffic_needs_a_matching_plan():
             "rank_order": 1, "reduce_mode": 0}
     assert bench.recorded_traffic("gemm_rs_pair_kernel", "ffn_w8_m4096", plan) is None
     assert bench.recorded_traffic("gemm_rs_pair_kernel", "no_such_workload", plan) is None
+
+
+def test_kernel_identity_ignores_comments_but_not_code():
+    src = 'int f(int x) { // a comment\n  return x + 1; /* another */\n}\nconst char *s = "a // b";\n'
+    edited_comment = src.replace("a comment", "edited")
+    edited_code = src.replace("x + 1", "x + 2")
+    assert bench.code_only(src) == bench.code_only(edited_comment)
+    assert bench.code_only(src) != bench.code_only(edited_code)
+    assert '"a // b"' in bench.code_only(src)          # a string literal is kept whole
+    assert "comment" not in bench.code_only(src) and "another" not in bench.code_only(src)
