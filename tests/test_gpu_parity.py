@@ -288,3 +288,25 @@ def test_chunked_two_stream_baseline_matches_oracle():
         run()
         torch.cuda.synchronize()
         np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, C, 0.5, 1.0, y_dtype))
+
+
+DEGENERATE = [
+    # W, M, N, Kpr          what it covers
+    (4, 4, 8, 8),         # one row per chunk, N = 8 (one 16-byte column group), K/W = 8
+    (2, 256, 8, 16),      # N = 8 with full row tiles, K/W = 16 (a quarter of a k-block)
+    (8, 1024, 24, 8),     # K/W = 8 on the CTA-pair tile, N of three 8-column groups
+    (16, 16, 264, 8),     # W = 16, one row per chunk, ragged N
+]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("W,M,N,Kpr", DEGENERATE)
+def test_degenerate_shapes_bit_exact(W, M, N, Kpr, tile, mode):
+    """Sizes at the edges of the layout rules: the smallest K per rank and N
+    (TMA boxes larger than the tensor, zero fill), one row per chunk, W = 16."""
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
+    y, _, op = run_gpu(A, B, C, W, M, N, Kpr, 0.5, 1.0, "fp32", tile_m=tile[0], tile_n=tile[1],
+                       reduce_mode=mode, poison=True, calls=2)
+    np.testing.assert_array_equal(y, oracle_y(A, B, C, 0.5, 1.0, "fp32"))
+    assert int(op.flags_view().abs().sum()) == 0
