@@ -24,6 +24,8 @@ SHAPES = [
     (8, 2048, 512, 128),           # eight ranks, one 256-row tile per chunk
     (16, 16 * 256, 64, 64),        # W = 16
     (4, 2048, 1000, 136),          # two 256-row tiles per chunk, ragged N
+    (2, 512, 8, 8),                # N = 8 and K = 8: TMA boxes larger than the tensors
+    (4, 1024, 16, 24),             # small N and K, four ranks
 ]
 
 
