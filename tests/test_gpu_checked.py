@@ -68,6 +68,21 @@ for (W, M, N, K) in [(2, 512, 256, 256), (3, 768, 264, 200), (1, 256, 72, 64),
             1.0, y_dtype))
         ag_cases += 1
 print("checked ag cases", ag_cases)
+# M*N = 2^31 output elements: the 64-bit index arithmetic of the epilogue and folds
+W, M, N, Kpr = 2, 65536, 32768, 64
+A, B, _ = inputs(W, M, N, Kpr, "int")
+rows = np.array([0, 1, M // 2, M - 2, M - 1])
+ref = oracle_y(A, B, None, 1.0, 0.0, "fp32", rows=rows)
+for mode in (0, 1, 2):
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device="cuda:0")
+    b.gemm_rs_set_reduce_mode(op.handle, mode)
+    Y = op.run(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert op.status() == 0
+    np.testing.assert_array_equal(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref)
+    del Y, op
+    torch.cuda.empty_cache()
+print("checked big ok")
 """
 
 
@@ -79,6 +94,7 @@ def test_checked_build_finds_no_access_out_of_bounds():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
     assert "checked cases 144" in r.stdout
     assert "checked ag cases 12" in r.stdout
+    assert "checked big ok" in r.stdout
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])

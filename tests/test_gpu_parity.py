@@ -310,3 +310,25 @@ def test_degenerate_shapes_bit_exact(W, M, N, Kpr, tile, mode):
                        reduce_mode=mode, poison=True, calls=2)
     np.testing.assert_array_equal(y, oracle_y(A, B, C, 0.5, 1.0, "fp32"))
     assert int(op.flags_view().abs().sum()) == 0
+
+
+def test_output_beyond_2_to_the_31_elements():
+    """M*N = 2^31 (Y 8.6 GB in fp32, partial workspace 17 GB): the epilogue's
+    and the folds' 64-bit index arithmetic, checked bit-exact on rows up to
+    the last one, with small K so the call is short."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import sample_rows
+    W, M, N, Kpr = 2, 65536, 32768, 64
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    dev = torch.device("cuda", 0)
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.0, "fp32", device=dev)
+    Y = op.run(A.to(dev), B.to(dev))
+    torch.cuda.synchronize()
+    assert op.status() == b.GEMM_RS_OK
+    rows = np.unique(np.concatenate([sample_rows(M, W, n_random=4, n_boundaries=2),
+                                     [M - 1, M - 2, M // 2 + 1]]))
+    y = Y[torch.from_numpy(rows).to(dev)].cpu().numpy()
+    np.testing.assert_array_equal(y, oracle_y(A, B, None, 1.0, 0.0, "fp32", rows=rows))
+    assert int(op.flags_view().abs().sum()) == 0
+    del Y, op
+    torch.cuda.empty_cache()
