@@ -221,6 +221,18 @@ def gemm_rs_run_noalloc(M, N, K, W, alpha, beta, y_dtype, A, B, C, Y, stream=0) 
 GEMM_RS_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
+def _cuda_device(device):
+    """A CUDA torch.device with an index: None or "cuda" mean the current device,
+    so that it compares equal to the device of the tensors placed there."""
+    import torch
+    d = torch.device("cuda") if device is None else torch.device(device)
+    if d.type != "cuda":
+        raise ValueError(f"the library runs on CUDA devices, not {d}")
+    if d.index is None:
+        d = torch.device("cuda", torch.cuda.current_device())
+    return d
+
+
 def _stream_ptr(stream) -> int:
     import torch
     if stream is None:
@@ -243,8 +255,7 @@ class GemmRS:
         lib()
         self.M, self.N, self.K, self.W = M, N, K, W
         self.alpha, self.beta, self.y_dtype = alpha, beta, y_dtype
-        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
-            else torch.device(device)
+        self.device = _cuda_device(device)
         nbytes = gemm_rs_workspace_bytes(M, N, K, W)
         if nbytes == 0:
             _check(GEMM_RS_ERR_SHAPE)
@@ -376,8 +387,7 @@ class AgGemm:
         lib()
         self.M, self.N, self.K, self.W = M, N, K, W
         self.alpha, self.y_dtype = alpha, y_dtype
-        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
-            else torch.device(device)
+        self.device = _cuda_device(device)
         nbytes = ag_gemm_workspace_bytes(M, N, K, W)
         if nbytes == 0:
             lib().ag_gemm_create(ctypes.byref(ctypes.c_void_p()), M, N, K, W, alpha, 0, None, 0, None)

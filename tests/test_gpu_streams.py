@@ -72,3 +72,21 @@ def test_two_handles_on_two_streams_at_once():
         assert ops[k].status(streams[k]) == b.GEMM_RS_OK
         for Y in outs[k]:
             np.testing.assert_array_equal(to_np_y(Y), refs[k])
+
+
+def test_device_given_without_an_index():
+    """device="cuda" (no index) means the current device: tensors on cuda:0 are
+    accepted, as in the usage example."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 2, 256, 256, 64
+    A, B, _ = inputs(W, M, N, Kpr, "int")
+    op = b.GemmRS(M, N, W * Kpr, W, alpha=1.0, beta=0.0, y_dtype="fp32", device="cuda")
+    Y = op.run(A.cuda(), B.cuda())
+    assert op.status() == b.GEMM_RS_OK
+    np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
+    ag = b.AgGemm(512, 64, 64, 2, 1.0, "fp32", device="cuda")
+    X = torch.zeros(512, 64, dtype=torch.bfloat16, device="cuda")
+    B1 = torch.zeros(2, 64, 64, dtype=torch.bfloat16, device="cuda")
+    H = ag.run(X, B1)
+    assert ag.status() == b.GEMM_RS_OK
+    assert not H.float().abs().sum().item()
