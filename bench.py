@@ -965,6 +965,15 @@ def run_ffn(args):
     rs_ms = time_loop(lambda: rs.run(H, B2d, None, Y, stream), args.steps, stream)
     if ag.status(stream) != 0 or rs.status(stream) != 0:
         raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+    if args.skip_extras:
+        print(json.dumps({"metric": FFN_METRIC, "value": flops / (ms_step / 1e3) / 1e12,
+                          "unit": "TFLOP/s", "ms_per_step": ms_step,
+                          "stages": {"ag_gemm_ms": ag_ms, "gemm_rs_ms": rs_ms},
+                          "clocks": sampler.stop(),
+                          "note": "profiling run: the fused chain only"}))
+        ag.close()
+        rs.close()
+        return 0
 
     # unfused chain: gather copy, bmm, bmm into fp32 partials, the reduce kernel
     G = torch.empty((wa.W, wa.M, wa.K), dtype=torch.bfloat16, device=dev)
