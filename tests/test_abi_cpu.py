@@ -41,6 +41,19 @@ def test_exports_every_declared_symbol(b):
     assert not missing, missing
 
 
+def test_checked_build_exports_the_same_symbols():
+    """The bounds-checked build is the same ABI: every declared symbol is there,
+    and its version string names the flavour."""
+    import ctypes
+    from tensor_gemm_reduce_tcgen05_gb300 import build
+    path = build.build(checked=True)
+    L = ctypes.CDLL(path)
+    missing = [n for n in _declared() if not hasattr(L, n)]
+    assert not missing, missing
+    L.gemm_rs_version.restype = ctypes.c_char_p
+    assert b"checked" in L.gemm_rs_version()
+
+
 @pytest.mark.parametrize("path", ["gemm_rs.h", "ag_gemm.h"])
 def test_no_torch_types_in_header(path):
     text = open(os.path.join(ROOT, "include", path)).read()
