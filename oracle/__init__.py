@@ -51,15 +51,17 @@ def _load():
         lib.oracle_gemm_rs.restype = i32
         lib.oracle_gemm_rs.argtypes = [i32, i64, i64, i64, f32, f32, vp, vp, vp,
                                        i32, vp, i64, vp, vp, i32]
-        lib.oracle_schedule.restype = i64
-        lib.oracle_schedule.argtypes = [i32, i64, i64, i32, i32, i32, i32, i32, vp, i64]
+        lib.oracle_chunk_order.restype = i32
+        lib.oracle_chunk_order.argtypes = [i32, vp]
+        lib.oracle_tile_chunk.restype = i64
+        lib.oracle_tile_chunk.argtypes = [i32, i64, i32, vp, i64]
         lib.oracle_gemm_rs_two_level.restype = i32
         lib.oracle_gemm_rs_two_level.argtypes = [i32, i64, i64, i64, f32, f32, vp, vp, vp,
                                                  i32, vp, i64, vp, vp, i32, i32]
         lib.oracle_ag_gemm.restype = i32
         lib.oracle_ag_gemm.argtypes = [i32, i64, i64, i64, f32, vp, vp, i32, vp, i64, vp, vp]
-        lib.oracle_ag_schedule.restype = i64
-        lib.oracle_ag_schedule.argtypes = [i32, i64, i64, i32, i32, vp, i64]
+        lib.oracle_ag_chunk_order.restype = i32
+        lib.oracle_ag_chunk_order.argtypes = [i32, vp]
         lib.oracle_row_chunk.restype = i32
         lib.oracle_row_chunk.argtypes = [i32, i64, vp, vp]
         lib.oracle_bf16_from_float.restype = None
@@ -115,20 +117,23 @@ def gemm_rs(A: np.ndarray, B: np.ndarray, C: np.ndarray | None, alpha: float, be
     return out
 
 
-def schedule(W: int, M: int, N: int, BM: int, BN: int, G: int = 0, RG: int = 0,
-             order: str = "interleaved") -> np.ndarray:
-    """Global tile order as an int32 [W*nM*nN, 3] array of (r, mt, nt).
-    G = column tiles per group (0: one group); RG = row tiles per sweep (0: whole chunk);
-    order = "interleaved" (the W ranks side by side) or "sequential" (one rank after
-    another)."""
-    if order not in ("interleaved", "sequential"):
-        raise ValueError(f"unknown rank order {order!r}")
-    nM, nN = -(-M // BM), -(-N // BN)
-    out = np.zeros((W * nM * nN, 3), dtype=np.int32)
-    n = _load().oracle_schedule(W, M, N, BM, BN, G, RG, 1 if order == "sequential" else 0,
-                                out.ctypes.data, out.shape[0])
+def chunk_order(W: int) -> np.ndarray:
+    """The rank-offset swizzle: an int32 [W, W] array whose row r lists the
+    chunks rank r writes, step by step (remote chunks first, its own last)."""
+    out = np.zeros((W, W), dtype=np.int32)
+    if W < 1 or _load().oracle_chunk_order(W, out.ctypes.data) != 0:
+        raise ValueError(f"oracle_chunk_order rejected W = {W}")
+    return out
+
+
+def tile_chunk(W: int, M: int, BM: int) -> np.ndarray:
+    """The chunk each row tile of BM rows goes to (the chunk of its first row),
+    as an int32 array of ceil(M/BM) entries."""
+    nM = -(-M // BM) if BM > 0 else 0
+    out = np.zeros(max(nM, 1), dtype=np.int32)
+    n = _load().oracle_tile_chunk(W, M, BM, out.ctypes.data, out.shape[0])
     if n < 0:
-        raise ValueError(f"oracle_schedule rejected its arguments (rc={n})")
+        raise ValueError(f"oracle_tile_chunk rejected its arguments (rc={n})")
     return out[:n]
 
 
@@ -180,11 +185,11 @@ def ag_gemm(X_bits: np.ndarray, B1_bits: np.ndarray, alpha: float, y_dtype: str,
     return out
 
 
-def ag_schedule(W: int, M: int, N: int, BM: int, BN: int) -> np.ndarray:
-    """AG+GEMM tile order as an int32 [W*T, 3] array of (r, mt, nt)."""
-    nM, nN = M // BM, -(-N // BN)
-    out = np.zeros((W * nM * nN, 3), dtype=np.int32)
-    n = _load().oracle_ag_schedule(W, M, N, BM, BN, out.ctypes.data, out.shape[0])
-    if n < 0:
-        raise ValueError(f"oracle_ag_schedule rejected its arguments (rc={n})")
-    return out[:n]
+def ag_chunk_order(W: int) -> np.ndarray:
+    """The AG+GEMM consumption order: an int32 [W, W] array whose row r lists
+    the chunks of the gathered rows in the order rank r takes them (its own
+    first)."""
+    out = np.zeros((W, W), dtype=np.int32)
+    if W < 1 or _load().oracle_ag_chunk_order(W, out.ctypes.data) != 0:
+        raise ValueError(f"oracle_ag_chunk_order rejected W = {W}")
+    return out

@@ -21,8 +21,8 @@
  *   The pages give no summation order; this is the reading taken.
  * - H is [W][M][N]: rank r's full-M output of its columns.
  *
- * The tile order (oracle_ag_schedule) is written out from the same pages: a
- * thread block waits for its tile's signal in the order the tiles are sent
+ * The chunk order (oracle_ag_chunk_order) is written out from the same pages:
+ * a thread block waits for its tile's signal in the order the tiles are sent
  * ("flux精读" §3, the AllGather GEMM paragraph), and a rank starts with the
  * rows it already holds ("flux精读" §4.1: each rank starts at its own chunk).
  *
@@ -98,38 +98,22 @@ int oracle_ag_gemm(int W, int64_t M, int64_t N, int64_t K, float alpha, const ui
 }
 
 /*
- * The AG+GEMM tile order, built by enumeration:
- *  - Output tiles of rank r are (mt, nt) with mt < M/BM and nt < ceil(N/BN);
- *    a row tile lies in one chunk (BM divides M/W): chunk(mt) = mt*BM / (M/W).
- *  - Rank r takes its chunks in the order (r+s) mod W, s = 0 .. W-1: the rows
- *    it holds first, then the chunks in the order they are sent to it.
- *  - Inside a chunk, for each column tile, the chunk's row tiles ascending.
- *  - The ranks run one after another: entry r*T + p is rank r's p-th tile
- *    (T = tiles per rank).
- * Writes (r, mt, nt) triples.  Returns W*T, -1 on bad arguments, or -2 if
- * cap (in entries) is too small.
+ * The order in which rank r consumes the W chunks of the gathered rows: its
+ * own chunk first, then the others in rank order after it, wrapping:
+ * (r + s) mod W at step s = 0 .. W-1 ("flux精读" §4.1: each rank starts at
+ * its own chunk, as printed for ranks 0 and 1; §3: the GEMM blocks take their
+ * tiles in the order the chunks are sent).  The order of the tiles inside a
+ * chunk and how the ranks share one device are the library's choices; the
+ * tests check them against this order.
+ *
+ * Writes out[r*W + s].  Returns 0, or -1 on bad arguments.
  */
-int64_t oracle_ag_schedule(int W, int64_t M, int64_t N, int BM, int BN, int32_t *out, int64_t cap)
+int oracle_ag_chunk_order(int W, int32_t *out)
 {
-    if (W < 1 || M < 1 || N < 1 || BM < 1 || BN < 1 || M % W != 0 || (M / W) % BM != 0)
+    if (W < 1 || out == NULL)
         return -1;
-    const int64_t R = M / W;
-    const int64_t cnt = R / BM; /* row tiles per chunk */
-    const int64_t nN = (N + BN - 1) / BN;
-    const int64_t T = (M / BM) * nN;
-    if (cap < W * T)
-        return -2;
-    int64_t g = 0;
     for (int r = 0; r < W; ++r)
-        for (int s = 0; s < W; ++s) {
-            const int64_t c = (r + s) % W;
-            for (int64_t nt = 0; nt < nN; ++nt)
-                for (int64_t i = 0; i < cnt; ++i) {
-                    out[3 * g] = r;
-                    out[3 * g + 1] = (int32_t)(c * cnt + i);
-                    out[3 * g + 2] = (int32_t)nt;
-                    ++g;
-                }
-        }
-    return g;
+        for (int s = 0; s < W; ++s)
+            out[r * W + s] = (r + s) % W;
+    return 0;
 }

@@ -29,10 +29,12 @@
  *   order: y = p_0, then y = y + p_r for r = 1 .. W-1.  A bf16 output is the
  *   round-to-nearest-even of y.
  *
- * The tile schedule (oracle_schedule) is written out from the swizzle rule
- * ("flux实现：sm80 gemm+rs", section "gemmrs版本的swizzle如何编排": remote
- * chunks first, the local chunk last; "flux精读" §4.1: each rank is offset
- * by its rank so that no two ranks write the same chunk at the same step).
+ * The swizzle (oracle_chunk_order, oracle_tile_chunk) is what the pages fix
+ * of the tile order and no more: each rank's chunk order, remote chunks first
+ * and the local chunk last ("flux实现：sm80 gemm+rs", section
+ * "gemmrs版本的swizzle如何编排"), each rank offset by its rank so that no two
+ * ranks write the same chunk at the same step ("flux精读" §4.1), and the
+ * chunk each row tile goes to.
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC.  FP contraction
  * stays off so that the result is the same on x86-64 and aarch64.
@@ -215,90 +217,56 @@ int oracle_row_chunk(int W, int64_t M, int32_t *chunk, int64_t *row_in_chunk)
 }
 
 /*
- * The tile schedule, built by enumeration:
- *  - Output tiles are (mt, nt) with mt < ceil(M/BM) and nt < ceil(N/BN).
- *  - A tile belongs to the chunk of its first row: key(mt) = (mt*BM) / R.
- *  - Rank r visits chunks in the order (r+1+s) mod W for s = 0 .. W-1, so its
- *    own chunk r comes last.
- *  - The column tiles form groups of G consecutive tiles (G <= 0 or G >= nN: a
- *    single group).  For each group, in order, the rank runs all W steps.
- *    Inside a group of gn tiles the rank starts at the group's tile
- *    ((W-r) mod W)*gn/W and wraps around within the group.  In a step, the
- *    chunk's row tiles (ascending) are split into row groups of RG tiles
- *    (RG <= 0: the whole chunk).  Each row group is one forward sweep over the
- *    group's column tiles.  For each column tile a sweep takes the row group's
- *    tiles in ascending order.
- *  - seq == 0: the W ranks run side by side: entry p*W + r of the global order
- *    is the p-th tile of rank r.  seq != 0: for each column group in turn, the
- *    ranks run one after another: the group's block of the global order holds
- *    rank 0's tiles of the group (its nM*gn entries in its own order), then
- *    rank 1's, and so on.
- * Writes (r, mt, nt) triples to out[3*g .. 3*g+2].  Returns the number of
- * entries W*nM*nN, -1 on bad arguments, or -2 if cap (in entries) is too small.
+ * The rank-offset swizzle, as the pages define it: the order in which each
+ * rank writes the W chunks of its output.  Rank r computes the remote chunks
+ * first and its own chunk r last ("flux实现：sm80 gemm+rs", section
+ * "gemmrs版本的swizzle如何编排"), and each rank starts one chunk further on
+ * than the rank before it, so that at no step do two ranks write the same
+ * chunk ("flux精读" §4.1, where rank 1 writes ranks 1..7 and then 0).  Joined,
+ * the two passages give chunk (r + 1 + s) mod W at step s = 0 .. W-1.
+ *
+ * The pages fix nothing finer than this: not the order of the tiles inside a
+ * chunk, nor how the W ranks share one device.  Those are the library's
+ * choices, and the tests check them against this order and the properties
+ * the pages state, not against an enumeration here.
+ *
+ * Writes out[r*W + s] for r, s = 0 .. W-1.  Returns 0, or -1 on bad arguments.
  */
-int64_t oracle_schedule(int W, int64_t M, int64_t N, int BM, int BN, int G, int RG, int seq,
-                        int32_t *out, int64_t cap)
+int oracle_chunk_order(int W, int32_t *out)
 {
-    if (W < 1 || M < 1 || N < 1 || BM < 1 || BN < 1 || M % W != 0)
+    if (W < 1 || out == NULL)
         return -1;
-    const int64_t R = M / W;
-    const int64_t nM = (M + BM - 1) / BM;
-    const int64_t nN = (N + BN - 1) / BN;
-    const int64_t T = nM * nN;
-    if (cap < W * T)
-        return -2;
-    int32_t *list = (int32_t *)malloc((size_t)T * 2 * sizeof(int32_t));
-    int64_t *rows = (int64_t *)malloc((size_t)nM * sizeof(int64_t));
-    if (list == NULL || rows == NULL) {
-        free(list);
-        free(rows);
-        return -1;
-    }
-    const int64_t group = (G <= 0 || G >= nN) ? nN : G;
     for (int r = 0; r < W; ++r) {
-        int64_t p = 0;
-        for (int64_t g0 = 0; g0 < nN; g0 += group) {
-            const int64_t gn = (nN - g0 < group) ? nN - g0 : group;
-            const int64_t rot = ((int64_t)((W - r) % W) * gn) / W;
-            for (int s = 0; s < W; ++s) {
-                const int64_t c = (r + 1 + s) % W;
-                /* the chunk's row tiles, ascending */
-                int64_t n_rows = 0;
-                for (int64_t mt = 0; mt < nM; ++mt)
-                    if ((mt * BM) / R == c)
-                        rows[n_rows++] = mt;
-                const int64_t rgs = (RG <= 0 || RG > n_rows) ? n_rows : RG;
-                for (int64_t r0 = 0; r0 < n_rows; r0 += rgs) {
-                    const int64_t r1 = (r0 + rgs < n_rows) ? r0 + rgs : n_rows;
-                    for (int64_t j = 0; j < gn; ++j) {
-                        const int64_t nt = g0 + (j + rot) % gn;
-                        for (int64_t i = r0; i < r1; ++i) {
-                            list[2 * p] = (int32_t)rows[i];
-                            list[2 * p + 1] = (int32_t)nt;
-                            ++p;
-                        }
-                    }
-                }
-            }
-        }
-        if (p != T) {
-            free(list);
-            free(rows);
-            return -1;
-        }
-        for (int64_t q = 0; q < T; ++q) {
-            int64_t g = q * W + r;
-            if (seq) {
-                const int64_t k = q / (nM * group);            /* column group of entry q */
-                const int64_t gn = (nN - k * group < group) ? nN - k * group : group;
-                g = k * W * nM * group + r * nM * gn + (q - k * nM * group);
-            }
-            out[3 * g] = r;
-            out[3 * g + 1] = list[2 * q];
-            out[3 * g + 2] = list[2 * q + 1];
+        /* remote chunks in rank order after r, wrapping, then r itself */
+        int c = r;
+        for (int s = 0; s < W; ++s) {
+            c = (c + 1 == W) ? 0 : c + 1;
+            out[r * W + s] = c;
         }
     }
-    free(list);
-    free(rows);
-    return W * T;
+    return 0;
+}
+
+/*
+ * The chunk a row tile of BM rows is sent to.  The pages' unit of
+ * communication is one output tile ("flux实现：sm80 gemm+rs": the scatter
+ * store goes through a ReduceScatterOp over kM x kN tiles) and a chunk is
+ * M/W contiguous rows; where a tile straddles two chunks the reading taken
+ * is that it goes with the chunk of its first row.  Writes out[mt] for
+ * mt = 0 .. ceil(M/BM)-1.  Returns the number of row tiles, -1 on bad
+ * arguments, or -2 if cap is too small.
+ */
+int64_t oracle_tile_chunk(int W, int64_t M, int BM, int32_t *out, int64_t cap)
+{
+    if (W < 1 || M < 1 || BM < 1 || M % W != 0 || out == NULL)
+        return -1;
+    const int64_t nM = (M + BM - 1) / BM;
+    if (cap < nM)
+        return -2;
+    const int64_t R = M / W;
+    for (int64_t mt = 0; mt < nM; ++mt) {
+        const int64_t first_row = mt * BM;
+        out[mt] = (int32_t)(first_row / R);
+    }
+    return nM;
 }

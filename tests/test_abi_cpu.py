@@ -1,7 +1,8 @@
 """C-ABI checks that need no GPU: the library loads, exports every symbol
 include/gemm_rs.h and include/ag_gemm.h declare, validates arguments before
-touching the device, and its host-side tile schedules equal the oracle's bit
-for bit."""
+touching the device, and its host-side tile schedules follow the pages'
+swizzle (checked against the oracle's chunk order, schedule_props.py) and
+keep the arrival order its chain reduction relies on."""
 import os
 import re
 
@@ -9,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+from schedule_props import check_ag_schedule, check_rs_schedule
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gemm_rs.h")
@@ -65,22 +67,107 @@ def test_version(b):
     assert "sm_103a" in b.gemm_rs_version()
 
 
-@pytest.mark.parametrize("W,M,N,bn", [
+SCHEDULE_SHAPES = [
     (2, 256, 256, 256), (8, 4096, 4096, 256), (8, 8192, 8192, 256), (8, 64, 8192, 64),
     (4, 16384, 5120, 256), (3, 300, 520, 128), (1, 200, 72, 64), (5, 640, 1000, 256),
     (16, 16 * 7, 64, 64), (7, 7 * 129, 264, 128),
-])
-def test_schedule_matches_oracle(b, W, M, N, bn):
-    orders = ((b.GEMM_RS_RANKS_INTERLEAVED, "interleaved"), (b.GEMM_RS_RANKS_SEQUENTIAL, "sequential"),
-              (b.GEMM_RS_RANKS_DEFAULT, "sequential"))
-    for G, RG in ((0, 0), (1, 0), (2, 3), (5, 1), (0, 2), (3, 5)):
-        for code, order in orders:
-            ours = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG, code)
-            ref = oracle.schedule(W, M, N, 128, bn, G, RG, order)
-            np.testing.assert_array_equal(ours, ref)
-            # the CTA-pair kernel walks 256-row tiles
-            np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 256, 256, G, RG, code),
-                                          oracle.schedule(W, M, N, 256, 256, G, RG, order))
+]
+SCHEDULE_GROUPS = ((0, 0), (1, 0), (2, 3), (5, 1), (0, 2), (3, 5), (4, 0), (8, 0))
+
+
+@pytest.mark.parametrize("W,M,N,bn", SCHEDULE_SHAPES)
+def test_schedule_follows_the_swizzle(b, W, M, N, bn):
+    """Every plan of the library, both tile heights and both rank orders: each
+    rank-tile once, each rank's chunks in the pages' order in every column,
+    and (ranks side by side) W different chunks at every step."""
+    for G, RG in SCHEDULE_GROUPS:
+        for code in (b.GEMM_RS_RANKS_INTERLEAVED, b.GEMM_RS_RANKS_SEQUENTIAL,
+                     b.GEMM_RS_RANKS_DEFAULT):
+            inter = code == b.GEMM_RS_RANKS_INTERLEAVED
+            for bm, tbn in ((128, bn), (256, 256)):
+                check_rs_schedule(b.gemm_rs_schedule(M, N, W, bm, tbn, G, RG, code), W, M, N,
+                                  bm, tbn, inter)
+
+
+@pytest.mark.parametrize("W,M,N,bn", SCHEDULE_SHAPES)
+def test_rank_orders_keep_each_ranks_own_order(b, W, M, N, bn):
+    """The two rank orders differ only in how the ranks share the device: each
+    rank's own sequence of tiles is the same, and with the ranks one after
+    another each column group is one block per rank, in rank order."""
+    for G, RG in SCHEDULE_GROUPS:
+        side = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG, b.GEMM_RS_RANKS_INTERLEAVED)
+        seq = b.gemm_rs_schedule(M, N, W, 128, bn, G, RG, b.GEMM_RS_RANKS_SEQUENTIAL)
+        np.testing.assert_array_equal(b.gemm_rs_schedule(M, N, W, 128, bn, G, RG,
+                                                         b.GEMM_RS_RANKS_DEFAULT), seq)
+        nM, nN = -(-M // 128), -(-N // bn)
+        assert np.array_equal(side[:, 0], np.tile(np.arange(W), nM * nN))
+        for r in range(W):
+            assert np.array_equal(seq[seq[:, 0] == r], side[side[:, 0] == r])
+        group = nN if G <= 0 or G >= nN else G
+        start = 0
+        for g0 in range(0, nN, group):
+            gn = min(group, nN - g0)
+            block = seq[start:start + W * nM * gn]
+            assert np.array_equal(block[:, 0], np.repeat(np.arange(W), nM * gn))
+            assert set(block[:, 2].tolist()) == set(range(g0, g0 + gn))
+            start += W * nM * gn
+
+
+@pytest.mark.parametrize("W,M,N,BM,BN,G", [
+    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
+    (2, 1024, 2048, 128, 256, 0), (8, 4096, 4096, 256, 256, 8), (8, 8192, 8192, 256, 256, 16),
+    (4, 16384, 5120, 256, 256, 8)])
+def test_interleaved_contributions_arrive_in_step_order(b, W, M, N, BM, BN, G):
+    """Ranks side by side: every output tile's W contributions come in step
+    order (the order the chain reduction folds them in), each at least about
+    (1 - 1/W) of a step after the previous one, also with column groups."""
+    sched = b.gemm_rs_schedule(M, N, W, BM, BN, G, 0, b.GEMM_RS_RANKS_INTERLEAVED)
+    nM, nN = -(-M // BM), -(-N // BN)
+    group = nN if G <= 0 or G >= nN else G
+    key = oracle.tile_chunk(W, M, BM)
+    order = oracle.chunk_order(W)
+    seen = {}
+    for g, (r, mt, nt) in enumerate(sched.tolist()):
+        seen.setdefault((mt, nt), []).append((g, r))
+    for (mt, nt), lst in seen.items():
+        steps = [order[r].tolist().index(key[mt]) for (_, r) in lst]
+        assert steps == list(range(W))
+        g0 = (nt // group) * group
+        per_step = nM * min(group, nN - g0)
+        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
+        assert min(gaps) >= per_step * (W - 1) // W - W
+
+
+@pytest.mark.parametrize("W,M,N,BM,BN,G", [
+    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
+    (8, 4096, 4096, 256, 256, 8), (8, 8192, 8192, 256, 256, 4), (3, 300, 520, 128, 128, 0),
+    (5, 5 * 256, 1000, 128, 256, 2)])
+def test_sequential_contributions_arrive_in_rank_order(b, W, M, N, BM, BN, G):
+    """Ranks one after another: every output tile's contributions come in rank
+    order, at least T*(W-2)/W entries apart (T = a rank's tiles in the tile's
+    column group): the chain reduction then folds in rank order."""
+    sched = b.gemm_rs_schedule(M, N, W, BM, BN, G, 0, b.GEMM_RS_RANKS_SEQUENTIAL)
+    nM, nN = -(-M // BM), -(-N // BN)
+    group = nN if G <= 0 or G >= nN else G
+    seen = {}
+    for g, (r, mt, nt) in enumerate(sched.tolist()):
+        seen.setdefault((mt, nt), []).append((g, r))
+    for (mt, nt), lst in seen.items():
+        assert [r for _, r in lst] == list(range(W))
+        T = nM * min(group, nN - (nt // group) * group)
+        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
+        assert min(gaps) >= T * (W - 2) // W
+
+
+def test_ranks_start_on_different_columns_when_one_row_tile_holds_every_chunk(b):
+    """M = 64, W = 8: one row tile (keyed to chunk 0).  The library starts
+    rank r's sweep at column ((W-r) mod W)*nN/W, so the ranks side by side
+    begin on W different column tiles."""
+    W, M, N, BM, BN = 8, 64, 8192, 128, 64
+    sched = b.gemm_rs_schedule(M, N, W, BM, BN, 0, 0, b.GEMM_RS_RANKS_INTERLEAVED)
+    nN = N // BN
+    assert sched[:W, 2].tolist() == [(((W - r) % W) * nN) // W for r in range(W)]
+    assert len(set(sched[:W, 2].tolist())) == W
 
 
 def test_workspace_bytes(b):
@@ -150,8 +237,8 @@ def test_reduce_partials_validates(b):
 
 @pytest.mark.parametrize("W,M,N", [(1, 256, 72), (2, 512, 256), (8, 2048, 768), (8, 4096, 1792),
                                    (3, 1536, 1000), (16, 16 * 256, 64)])
-def test_ag_schedule_matches_oracle(b, W, M, N):
-    np.testing.assert_array_equal(b.ag_gemm_schedule(M, N, W), oracle.ag_schedule(W, M, N, 256, 256))
+def test_ag_schedule_follows_the_consumption_order(b, W, M, N):
+    check_ag_schedule(b.ag_gemm_schedule(M, N, W), W, M, N, 256, 256)
 
 
 def test_ag_shape_checks(b):

@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from helpers import assert_close, inputs, oracle_y, run_gpu, to_np_y
+from schedule_props import check_rs_schedule
 from tensor_gemm_reduce_tcgen05_gb300.inputs import (WORKLOADS, bf16_bits, sample_rows,
                                                      workload_inputs)
 
@@ -145,7 +146,12 @@ def test_twenty_calls_bit_identical_and_counters_reset(mode):
     assert_close(first.numpy(), oracle_y(A, B, None, 1.0, 0.0, "fp32"), "fp32", "20 calls")
 
 
-def test_device_schedule_record_matches_schedule_and_oracle():
+def test_device_schedule_record_follows_the_swizzle():
+    """The order the kernel really walked (its device record) equals the
+    library's host schedule, and follows the pages' swizzle: each rank-tile
+    once, each rank's chunks in the oracle's chunk order in every column, W
+    distinct chunks per step with the ranks side by side.  Plans with column
+    groups, row groups and both rank orders, for both kernels."""
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
     for (W, M, N, Kpr, bm, bn, G, RG, ro) in [(8, 1024, 1024, 64, 128, 256, 0, 0, 0),
                                               (8, 1024, 1024, 64, 128, 256, 0, 0, 2),
@@ -155,6 +161,7 @@ def test_device_schedule_record_matches_schedule_and_oracle():
                                               (8, 4096, 1024, 64, 256, 256, 0, 0, 2),
                                               (8, 4096, 1024, 64, 256, 256, 0, 0, 1),
                                               (8, 4096, 2048, 64, 256, 256, 3, 1, 2),
+                                              (8, 4096, 2048, 64, 256, 256, 2, 0, 1),
                                               (4, 4096, 2048, 64, 256, 256, 0, 3, 0),
                                               (3, 300, 520, 64, 256, 256, 1, 0, 2)]:
         A, B, _ = inputs(W, M, N, Kpr, "int")
@@ -167,15 +174,13 @@ def test_device_schedule_record_matches_schedule_and_oracle():
         torch.cuda.synchronize()
         rec = rec.cpu().numpy()
         plan = op.plan
-        assert plan["rank_order"] == (b.GEMM_RS_RANKS_INTERLEAVED if ro == 2
+        inter = ro == 2
+        assert plan["rank_order"] == (b.GEMM_RS_RANKS_INTERLEAVED if inter
                                       else b.GEMM_RS_RANKS_SEQUENTIAL)
-        order = "interleaved" if ro == 2 else "sequential"
         lib_sched = b.gemm_rs_schedule(M, N, W, bm, bn, plan["colgroup"], plan["rowgroup"],
                                        plan["rank_order"])
         np.testing.assert_array_equal(rec[:, :3], lib_sched)
-        np.testing.assert_array_equal(rec[:, :3],
-                                      oracle.schedule(W, M, N, bm, bn, plan["colgroup"],
-                                                      plan["rowgroup"], order))
+        check_rs_schedule(rec[:, :3], W, M, N, bm, bn, inter)
         grid = op.plan["grid"]
         workers = grid // 2 if bm == 256 else grid  # CTA pairs process one entry each
         np.testing.assert_array_equal(rec[:, 3], np.arange(rec.shape[0]) % workers)

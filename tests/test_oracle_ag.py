@@ -125,37 +125,11 @@ def _printed_orders():
     return orders
 
 
-def test_ag_schedule_is_the_printed_rank_offset_order():
+def test_ag_chunk_order_is_the_printed_rank_offset_order():
     """Each rank takes its chunks starting at its own, as printed for ranks 0
-    and 1; inside a chunk the column tiles run outer and the chunk's row tiles
-    ascend inner; the ranks run one after another."""
-    W, M, N, BM, BN = 8, 8 * 256, 768, 128, 256
-    sched = oracle.ag_schedule(W, M, N, BM, BN)
-    nM, nN = M // BM, -(-N // BN)
-    cnt = (M // W) // BM
-    assert sched.shape == (W * nM * nN, 3)
-    assert np.array_equal(sched[:, 0], np.repeat(np.arange(W), nM * nN))
-    keys = set(map(tuple, sched.tolist()))
-    assert keys == {(r, m, n) for r in range(W) for m in range(nM) for n in range(nN)}
-    for r, order in _printed_orders().items():
-        mine = sched[sched[:, 0] == r]
-        chunks = []
-        for (_, mt, _) in mine.tolist():
-            c = mt // cnt
-            if not chunks or chunks[-1] != c:
-                chunks.append(c)
-        assert chunks == order
-        first = mine[:nN * cnt]          # the local chunk: columns outer, rows inner
-        assert first[:, 2].tolist() == [n for n in range(nN) for _ in range(cnt)]
-        assert first[:, 1].tolist() == [r * cnt + i for _ in range(nN) for i in range(cnt)]
-    for r in range(W):
-        chunks = []
-        for (_, mt, _) in sched[sched[:, 0] == r].tolist():
-            if not chunks or chunks[-1] != mt // cnt:
-                chunks.append(mt // cnt)
-        assert chunks == [(r + s) % W for s in range(W)]
-
-
-def test_ag_schedule_rejects_tiles_that_straddle_chunks():
-    with pytest.raises(ValueError):
-        oracle.ag_schedule(4, 4 * 100, 256, 128, 256)
+    and 1 of eight ("flux精读" §4.1).  The other ranks and sizes are pinned by
+    the properties in test_oracle_schedule.py (every chunk once per rank, own
+    chunk first, W distinct chunks per step)."""
+    order = oracle.ag_chunk_order(8)
+    for r, seq in _printed_orders().items():
+        assert order[r].tolist() == seq

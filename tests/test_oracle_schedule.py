@@ -1,10 +1,13 @@
-"""Pins for the oracle's tile schedule (no GPU needed).
+"""Pins for the oracle's swizzle and for the schedule checks (no GPU needed).
 
-The schedule is checked against the order printed on the pages
-(tests/golden/swizzle_rank_offset_w8.txt) and against the properties that
-the pages state: remote chunks first and the local chunk last; each rank
-offset by its rank, so that the W ranks target W different chunks at every
-step; and every rank-tile visited exactly once.
+The oracle states what the pages fix of the tile order: each rank's chunk
+order (remote chunks first, the local chunk last, each rank offset by its
+rank) and the chunk each row tile goes to.  It is pinned here by the order
+printed on the pages (tests/golden/swizzle_rank_offset_w8.txt), by the
+properties the pages state (W distinct chunks at every step), and by the
+row-to-chunk partition.  The checks in schedule_props.py, which compare the
+library's schedules with the oracle, are pinned by planting mistakes in a
+correct schedule and seeing each one caught.
 """
 import os
 
@@ -12,6 +15,8 @@ import numpy as np
 import pytest
 
 import oracle
+from schedule_props import (ScheduleError, check_ag_schedule, check_chunk_orders,
+                            check_distinct_chunks_per_step, check_rs_schedule)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "swizzle_rank_offset_w8.txt")
 
@@ -28,171 +33,154 @@ def _printed_orders():
     return orders
 
 
-def _chunk_sequence(sched, W, M, BM, r):
-    """Chunk order of rank r, read off its tiles' chunk keys."""
-    R = M // W
-    seq = []
-    for (rr, mt, nt) in sched:
-        if rr != r:
-            continue
-        c = (mt * BM) // R
-        if not seq or seq[-1] != c:
-            seq.append(c)
-    return seq
-
-
-def test_matches_printed_rank_offset_order():
-    W, M, N, BM, BN = 8, 8 * 256, 512, 128, 256
-    sched = oracle.schedule(W, M, N, BM, BN)
+def test_chunk_order_matches_printed_rank_offset_order():
+    """"flux精读" §4.1 prints ranks 0 and 1 of eight starting at their own
+    chunk; "flux实现" moves the local chunk to the end.  So the oracle's
+    order with its last entry moved to the front is the printed one."""
+    order = oracle.chunk_order(8)
     printed = _printed_orders()
     assert set(printed) == {0, 1}
-    for r, order in printed.items():
-        seq = _chunk_sequence(sched, W, M, BM, r)
-        assert seq[-1] == r                      # local chunk last
-        assert [seq[-1]] + seq[:-1] == order      # = printed order, local moved to the front
+    for r, seq in printed.items():
+        mine = order[r].tolist()
+        assert mine[-1] == r
+        assert [mine[-1]] + mine[:-1] == seq
 
 
-@pytest.mark.parametrize("order", ["interleaved", "sequential"])
-@pytest.mark.parametrize("G,RG", [(0, 0), (1, 0), (3, 0), (0, 1), (2, 3)])
-@pytest.mark.parametrize("W,M,N,BM,BN", [
-    (2, 256, 256, 128, 256), (8, 4096, 4096, 128, 256), (4, 16384, 5120, 128, 256),
-    (8, 64, 8192, 128, 64), (3, 300, 520, 128, 128), (1, 200, 72, 128, 64),
-    (5, 5 * 128, 1000, 128, 256), (8, 4096, 4096, 256, 256),
-])
-def test_schedule_properties(W, M, N, BM, BN, G, RG, order):
-    sched = oracle.schedule(W, M, N, BM, BN, G, RG, order)
-    nM, nN = -(-M // BM), -(-N // BN)
-    assert sched.shape == (W * nM * nN, 3)
-    # every rank-tile exactly once
-    keys = set(map(tuple, sched.tolist()))
-    assert len(keys) == W * nM * nN
-    assert keys == {(r, m, n) for r in range(W) for m in range(nM) for n in range(nN)}
-    if order == "interleaved":
-        # ranks run side by side
-        assert np.array_equal(sched[:, 0], np.tile(np.arange(W), nM * nN))
-    else:
-        # per column group, one rank after another; each rank's own order unchanged
-        group = nN if G <= 0 or G >= nN else G
-        start = 0
-        for g0 in range(0, nN, group):
-            gn = min(group, nN - g0)
-            block = sched[start:start + W * nM * gn]
-            assert np.array_equal(block[:, 0], np.repeat(np.arange(W), nM * gn))
-            assert set(block[:, 2].tolist()) == set(range(g0, g0 + gn))
-            start += W * nM * gn
-        side = oracle.schedule(W, M, N, BM, BN, G, RG, "interleaved")
-        for r in range(W):
-            assert np.array_equal(sched[sched[:, 0] == r], side[side[:, 0] == r])
+def test_ag_chunk_order_is_the_printed_order():
+    """The all-gather side takes its own rows first: exactly the printed order."""
+    order = oracle.ag_chunk_order(8)
+    for r, seq in _printed_orders().items():
+        assert order[r].tolist() == seq
+
+
+@pytest.mark.parametrize("W", list(range(1, 17)))
+def test_chunk_order_properties(W):
+    """Each rank writes every chunk once, its own last; at every step the W
+    ranks write W different chunks (the point of the offset, §4.1); the
+    all-gather order is the same cycle with the local chunk moved to the
+    front."""
+    order = oracle.chunk_order(W)
+    ag = oracle.ag_chunk_order(W)
+    assert order.shape == (W, W)
+    for r in range(W):
+        assert sorted(order[r].tolist()) == list(range(W))
+        assert order[r, -1] == r
+        assert ag[r].tolist() == [r] + order[r, :-1].tolist()
+    for s in range(W):
+        assert sorted(order[:, s].tolist()) == list(range(W))
+        assert sorted(ag[:, s].tolist()) == list(range(W))
+
+
+def test_chunk_order_rejects_bad_w():
+    with pytest.raises(ValueError):
+        oracle.chunk_order(0)
+
+
+@pytest.mark.parametrize("W,M,BM", [(2, 256, 128), (8, 4096, 256), (8, 64, 128), (4, 400, 128),
+                                    (3, 300, 128), (16, 16 * 7, 128), (7, 7 * 129, 128),
+                                    (8, 8192, 256), (1, 200, 128)])
+def test_tile_chunk_is_the_chunk_of_the_first_row(W, M, BM):
+    """Each row tile goes with the chunk of its first row (the row-to-chunk
+    partition, pinned on its own); keys never decrease; when a chunk is a
+    whole number of tiles, each chunk gets exactly R/BM consecutive tiles."""
+    key = oracle.tile_chunk(W, M, BM)
+    chunk, _ = oracle.row_chunk(W, M)
+    nM = -(-M // BM)
+    assert key.shape == (nM,)
+    for mt in range(nM):
+        assert key[mt] == chunk[mt * BM]
+    assert np.all(np.diff(key) >= 0)
     R = M // W
-    groups = 1 if G <= 0 or G >= nN else -(-nN // G)
+    if R % BM == 0:
+        assert key.tolist() == [c for c in range(W) for _ in range(R // BM)]
+
+
+def test_tile_chunk_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.tile_chunk(3, 100, 128)  # M is not a multiple of W
+
+
+def _plain_rs_schedule(W, M, N, BM, BN, interleaved):
+    """A schedule built straight from the oracle's order: for each rank, for
+    each step, the chunk's row tiles, each swept over all columns."""
+    order = oracle.chunk_order(W)
+    key = oracle.tile_chunk(W, M, BM)
+    nN = -(-N // BN)
+    per_rank = []
     for r in range(W):
-        seq = _chunk_sequence(sched, W, M, BM, r)
-        present = {(mt * BM) // R for mt in range(nM)}
-        expect = [c for c in [(r + 1 + s) % W for s in range(W)] if c in present]
-        if len(expect) == 1:
-            assert seq == expect
-        else:
-            assert seq == expect * groups  # remote chunks first, local last, in every group
-    if R % BM == 0 and order == "interleaved":
-        # every position p: the W ranks target W distinct chunks
-        per_p = sched.reshape(nM * nN, W, 3)
-        for p in range(nM * nN):
-            chunks = {(int(mt) * BM) // R for (_, mt, _) in per_p[p]}
-            assert len(chunks) == W
+        lst = []
+        for c in order[r]:
+            for nt in range(nN):
+                for mt in np.nonzero(key == c)[0]:
+                    lst.append((r, int(mt), nt))
+        per_rank.append(lst)
+    if interleaved:
+        return np.array([per_rank[r][p] for p in range(len(per_rank[0])) for r in range(W)],
+                        dtype=np.int32)
+    return np.array([e for lst in per_rank for e in lst], dtype=np.int32)
 
 
-def test_every_sweep_runs_forward_from_the_rank_offset():
-    """Each step sweeps a rank's column tiles forward from ((W-r) mod W)*nN/W
-    (one column group)."""
-    W, M, N, BM, BN = 4, 4 * 128, 2048, 128, 256
-    sched = oracle.schedule(W, M, N, BM, BN)
-    nN = N // BN
-    for r in range(W):
-        cols = [int(nt) for (rr, mt, nt) in sched if rr == r]
-        rot = (((W - r) % W) * nN) // W
-        for s in range(W):
-            assert cols[s * nN:(s + 1) * nN] == [(j + rot) % nN for j in range(nN)]
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_checks_accept_a_plain_schedule(interleaved):
+    W, M, N, BM, BN = 8, 8 * 256, 768, 128, 256
+    check_rs_schedule(_plain_rs_schedule(W, M, N, BM, BN, interleaved), W, M, N, BM, BN,
+                      interleaved)
 
 
-def test_row_groups_sweep_all_columns_per_group():
-    """With row groups of 2 row tiles, a step of a 6-tile chunk makes three
-    forward sweeps over the column tiles, each covering its two row tiles for
-    every column."""
-    W, M, N, BM, BN, RG = 2, 2 * 6 * 128, 1024, 128, 256, 2
-    sched = oracle.schedule(W, M, N, BM, BN, 0, RG)
-    nN = N // BN
-    mine = [(int(mt), int(nt)) for (rr, mt, nt) in sched if rr == 0]
-    step0 = mine[:6 * nN]              # rank 0, step 0: chunk 1 (row tiles 6..11)
-    rot = (W * nN // W) % nN  # rank 0: offset ((W-0) mod W)*nN/W = 0
-    for k in range(3):
-        sweep = step0[k * 2 * nN:(k + 1) * 2 * nN]
-        cols = [sweep[2 * i][1] for i in range(nN)]
-        assert cols == [(j + rot) % nN for j in range(nN)]
-        for i in range(nN):
-            assert [sweep[2 * i][0], sweep[2 * i + 1][0]] == [6 + 2 * k, 7 + 2 * k]
-
-
-@pytest.mark.parametrize("W,M,N,BM,BN,G", [
-    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
-    (2, 1024, 2048, 128, 256, 0), (8, 4096, 4096, 256, 256, 8), (8, 8192, 8192, 256, 256, 16),
-    (4, 16384, 5120, 256, 256, 8)])
-def test_tile_contributions_arrive_in_step_order(W, M, N, BM, BN, G):
-    """For every output tile, the global order visits its W rank contributions
-    in step order, each at least (1 - 1/W) of a step after the previous one,
-    also with column groups (a step then covers one group's columns).  The
-    chain reduction folds them in that order."""
-    sched = oracle.schedule(W, M, N, BM, BN, G)
-    nM, nN = -(-M // BM), -(-N // BN)
-    group = nN if G <= 0 or G >= nN else G
+def _mutations(s, W, BM, M):
+    """Plausible mistakes in a tile order, each planted in a copy."""
     R = M // W
-    seen = {}
-    for g, (r, mt, nt) in enumerate(sched.tolist()):
-        seen.setdefault((mt, nt), []).append((g, r))
-    for (mt, nt), lst in seen.items():
-        c = (mt * BM) // R
-        steps = [((c - r - 1) % W) for (_, r) in lst]
-        assert steps == list(range(W))               # arrival order = step order
-        g0 = (nt // group) * group
-        per_step = nM * min(group, nN - g0)          # global entries per step of this group
-        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
-        assert min(gaps) >= per_step * (W - 1) // W - W  # ranks interleave: -1 per rank
+    out = {}
+    m = s.copy()
+    m[[0, 1]] = m[[1, 0]]                      # two entries of different ranks swapped
+    out["swap across ranks"] = m
+    m = s.copy()
+    m[5] = m[6]                                # a tile computed twice, another dropped
+    out["duplicate"] = m
+    r0 = np.nonzero(s[:, 0] == 0)[0]
+    m = s.copy()
+    last = r0[-1]
+    first = r0[0]
+    m[[first, last]] = m[[last, first]]        # rank 0's own chunk tile moved to the front
+    out["local chunk first"] = m
+    m = s.copy()
+    m[:, 1] = (m[:, 1] + R // BM) % (M // BM)  # every tile keyed one chunk further on
+    out["chunk shifted"] = m
+    m = s.copy()
+    m[:, 0] = (m[:, 0] + 1) % W                # ranks relabelled
+    out["rank relabelled"] = m
+    return out
 
 
-@pytest.mark.parametrize("W,M,N,BM,BN,G", [
-    (8, 4096, 4096, 256, 256, 0), (4, 16384, 5120, 256, 256, 0), (8, 8192, 8192, 256, 256, 0),
-    (8, 4096, 4096, 256, 256, 8), (3, 300, 520, 128, 128, 0), (5, 5 * 256, 1000, 128, 256, 2)])
-def test_sequential_ranks_arrive_in_rank_order(W, M, N, BM, BN, G):
-    """With the ranks one after another (per column group), every output tile
-    sees its W rank contributions in rank order 0 .. W-1 (the order the chain
-    reduction folds in, the same as the last arriver's).  Rank r+1 reaches a
-    tile at most one of its steps (T/W entries) earlier in its own pass over
-    the group than rank r, give or take the column offset, so consecutive
-    contributions lie at least T*(W-2)/W entries apart (T = a rank's tiles in
-    the tile's column group)."""
-    sched = oracle.schedule(W, M, N, BM, BN, G, 0, "sequential")
-    nM, nN = -(-M // BM), -(-N // BN)
-    group = nN if G <= 0 or G >= nN else G
-    seen = {}
-    for g, (r, mt, nt) in enumerate(sched.tolist()):
-        seen.setdefault((mt, nt), []).append((g, r))
-    for (mt, nt), lst in seen.items():
-        assert [r for _, r in lst] == list(range(W))
-        g0 = (nt // group) * group
-        T = nM * min(group, nN - g0)
-        gaps = [lst[i + 1][0] - lst[i][0] for i in range(W - 1)]
-        assert min(gaps) >= T * (W - 2) // W
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_checks_catch_planted_mistakes(interleaved):
+    W, M, N, BM, BN = 8, 8 * 256, 768, 128, 256
+    good = _plain_rs_schedule(W, M, N, BM, BN, interleaved)
+    for name, bad in _mutations(good, W, BM, M).items():
+        if name == "swap across ranks" and not interleaved:
+            bad = good.copy()
+            i, j = 0, W * 2 * 3  # rank 0 and rank 1 blocks exchange an entry
+            bad[[i, j]] = bad[[j, i]]
+        with pytest.raises(ScheduleError):
+            check_rs_schedule(bad, W, M, N, BM, BN, interleaved)
 
 
-def test_rank_column_offset_when_one_chunk_holds_all_tiles():
-    """M = 64, W = 8: chunks of 8 rows, one row tile (keyed to chunk 0).  Rank
-    r reaches chunk 0 at step s = W-1-r and sweeps forward from column
-    ((W-r) mod W)*nN/W, so the ranks start on different column tiles."""
-    W, M, N, BM, BN = 8, 64, 8192, 128, 64
-    sched = oracle.schedule(W, M, N, BM, BN)
-    nN = N // BN
-    first = sched[:W]
-    expect = []
-    for r in range(W):
-        expect.append((((W - r) % W) * nN) // W)  # one sweep per rank, forward
-    assert first[:, 2].tolist() == expect
-    assert len(set(expect)) == W
+def test_step_check_catches_two_ranks_on_one_chunk():
+    W, M, N, BM, BN = 4, 4 * 128, 512, 128, 256
+    good = _plain_rs_schedule(W, M, N, BM, BN, True)
+    key = oracle.tile_chunk(W, M, BM)
+    check_distinct_chunks_per_step(good, W, key)
+    bad = good.copy()
+    bad[1, 1] = bad[0, 1]
+    with pytest.raises(ScheduleError):
+        check_distinct_chunks_per_step(bad, W, key)
+
+
+def test_ag_check_catches_the_reduce_scatter_order():
+    """An AG order with the local chunk last (the reduce-scatter's) is caught."""
+    W, M, N, BM, BN = 4, 4 * 256, 512, 256, 256
+    rs = _plain_rs_schedule(W, M, N, BM, BN, False)
+    with pytest.raises(ScheduleError):
+        check_ag_schedule(rs, W, M, N, BM, BN)
+    key = oracle.tile_chunk(W, M, BM)
+    check_chunk_orders(rs, W, M, N, BM, BN, oracle.chunk_order(W), key)
