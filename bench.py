@@ -4,11 +4,18 @@
 
 One step is one pass of the whole hot path: one fused-kernel call that computes
 Y = sum_r (alpha*A_r*B_r + beta*C) over one batch of synthetic inputs.  By default
-the workload is ffn_w8_m4096: W = 8 logical ranks, M = N = 4096, K = 14336
-(1792 per rank), bf16 inputs, bf16 Y.  Inputs are seeded and synthetic (see
+the workload is ffn_w8_m8192_bias, the largest of the five: W = 8 logical ranks,
+M = N = 8192, K = 28672 (3584 per rank), alpha = 0.5, beta = 1 with a bf16 C,
+bf16 inputs, bf16 Y.  --workload picks another (ffn_w8_m4096, ffn_w4_m16384_x20,
+decode_w8_m64, tiny_w2).  Inputs are seeded and synthetic (see
 tensor_gemm_reduce_tcgen05_gb300/inputs.py) and stay resident in HBM during the
-timed region.  A + B (235 MB) plus the partial workspace (537 MB) are larger
+timed region.  A + B (940 MB) plus the partial workspace (2.1 GB) are larger
 than the 129 MB L2, so no L2 flush is needed between steps.
+
+The timed region is exactly --steps calls.  Right after it, the same calls run
+back to back for at least --sustain-seconds (the "sustained" figures): long
+enough for the 200 ms clock sampler to see the SM clock the kernel runs at once
+the board sits at its power cap.
 
 Rank 0 prints one JSON line.  It has the metric (fused TFLOP/s, whole job), the
 kernel's roofline fraction, the end-to-end figure through the public API with
@@ -433,6 +440,39 @@ def interleaved(arms, rounds, n, stream, timer=None):
     return {k: sum(v) / len(v) for k, v in per.items()}
 
 
+def sustained_run(step, w, stream, seconds: float, cold: bool, flush) -> dict:
+    """The fused calls back to back for at least `seconds`: blocks of calls
+    sized from a first probe block, each block timed with one event pair
+    (with an L2 flush before each call when the working set fits in L2, whose
+    time the calls' own events then exclude)."""
+    import torch
+    probe = max(1, min(200, int(0.05 / max(w.flops / 2.0e15, 1e-6))))
+    ms_probe = time_loop_b2b(step, probe, stream) if not cold else time_loop(step, probe, stream)
+    block = max(1, int(200.0 / max(ms_probe, 1e-3)))  # about 0.2 s per block
+    calls, total_ms, per_block = 0, 0.0, []
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        if cold:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(block)]
+            for a, b in evs:
+                flush()
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in evs)
+        else:
+            ms = time_loop_b2b(step, block, stream) * block
+        per_block.append(ms / block)
+        total_ms += ms
+        calls += block
+    ms_call = total_ms / calls
+    return {"calls": calls, "seconds": total_ms / 1e3, "ms_per_call": ms_call,
+            "ms_per_call_first_block": per_block[0], "ms_per_call_last_block": per_block[-1],
+            "tflops": w.flops / (ms_call / 1e3) / 1e12}
+
+
 def time_loop_b2b(fn, steps, stream):
     """Mean ms per call with the calls back to back (no events between them):
     what a caller that issues them in a row sees."""
@@ -507,13 +547,14 @@ def run_ours(args):
     def flush_l2():
         flush_buf.fill_(1.0)
 
-    sampler = ClockSampler(local)
-    sampler.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if op.status(stream) != 0:
         raise RuntimeError("device timeout during warm-up: " + binding.gemm_rs_last_error())
+    # clocks of the fused region: the timed steps and the sustained run after them
+    sampler = ClockSampler(local)
+    sampler.start()
 
     # ---- timed region: K fused calls, events around each launch
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -546,13 +587,31 @@ def run_ours(args):
     ms_step_max = max_over_ranks(dist, ms_step, dev)
     value = aggregate_throughput(w.flops, world, ms_step_max / 1e3) / 1e12
 
+    # ---- sustained: the same calls back to back for at least --sustain-seconds
+    sustained = None
+    if args.sustain_seconds > 0:
+        sustained = sustained_run(step, w, stream, args.sustain_seconds, cold, flush_l2)
+    clocks = sampler.stop()
+    if sustained is not None:
+        sustained["sm_mhz_median"] = clocks.get("sm_mhz")
+        sustained["samples_under_load"] = clocks.get("samples_under_load")
+        if clocks.get("sm_mhz"):
+            sustained["ms_x_ghz"] = sustained["ms_per_call"] * clocks["sm_mhz"] / 1e3
+        sustained["frac_of_sustained_peak"] = sustained["tflops"] / peaks["bf16_tflops_sustained"]
+        sustained["frac_of_burst_peak"] = sustained["tflops"] / peaks["bf16_tflops"]
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout in the sustained run: " + binding.gemm_rs_last_error())
+    sampler = ClockSampler(local)  # the rest of the run (baselines, ablations)
+    sampler.start()
+
     if args.skip_extras:
-        clocks = sampler.stop()
+        rest = sampler.stop()
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
                 "kernel_ms": kernel_avg_ms, "kernel_ms_median": kernel_median_ms,
                 "kernel_ms_min": kernel_min_ms, "config": workload_config(w), "plan": op.plan,
-                "clocks": clocks, "note": "profiling run: fused kernel only"}
+                "clocks": clocks, "sustained": sustained, "clocks_rest": rest,
+                "note": "profiling run: fused kernel only"}
         if rank == 0:
             print(json.dumps(line))
         op.close()
@@ -694,7 +753,7 @@ def run_ours(args):
     if op.status(stream) != 0:
         raise RuntimeError("device timeout in the reduce-mode comparison: " +
                            binding.gemm_rs_last_error())
-    clocks = sampler.stop()
+    clocks_rest = sampler.stop()
 
     # ---- roofline of the fused kernel (the only kernel of the step)
     flops_per_launch = float(w.flops)
@@ -705,7 +764,9 @@ def run_ours(args):
         achieved = flops_per_launch / (kernel_avg_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)"}
+                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+                "peak_sustained": peaks["bf16_tflops_sustained"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     else:
         achieved = bytes_per_launch / (kernel_avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -739,7 +800,9 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
-            "clocks": clocks,
+            "clocks": dict(clocks, region="the timed steps and the sustained run after them"),
+            "sustained": sustained,
+            "clocks_rest": clocks_rest,
             "cpu_baseline": cpu,
             "unfused": {"ms_per_step": unfused_ms,
                         "value": w.flops / (unfused_ms / 1e3) / 1e12,
@@ -1025,12 +1088,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ffn_w8_m4096")
+    ap.add_argument("--workload", default="ffn_w8_m8192_bias")
     ap.add_argument("--path", choices=["gemm_rs", "ag", "ffn"], default="gemm_rs",
                     help="gemm_rs: the fused GEMM + reduce-scatter (the default line); "
                          "ag: the fused all-gather + GEMM; ffn: both, chained")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sustain-seconds", type=float, default=None,
+                    help="after the timed steps, run the same calls back to back for at least "
+                         "this long and report their throughput and clock (0: skip; default 3, "
+                         "or 0 with --skip-extras)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--unfused-only", action="store_true",
                     help="run only the unfused arm (cuBLAS bmm into fp32 partials + reduce "
@@ -1042,6 +1109,8 @@ def main(argv=None):
     # At least three warm-up steps are always run; the JSON line reports the number run.
     args.warmup = max(3, args.warmup)
     args.steps = max(1, args.steps)
+    if args.sustain_seconds is None:
+        args.sustain_seconds = 0.0 if args.skip_extras else 3.0
     if args.impl == "reference":
         return run_reference(args)
     if args.path == "ag":

@@ -83,4 +83,43 @@ inline int encode_3d(CUtensorMap *map, const void *ptr, uint64_t d0, uint64_t d1
     return GEMM_RS_OK;
 }
 
+// B [W][K/W][N] bf16 as a 4D tensor {64, K/W, N/64, W}: column n = 64*a + j
+// is (j, a), so a box {64, 64, atoms, 1} is `atoms` consecutive 64-column
+// swizzle atoms of one 64-row k-block, laid out one after another (each 64
+// rows x 128 bytes, 128-byte swizzled), exactly as `atoms` 3D boxes would
+// be.  Needs N % 64 == 0; a box past the last atom reads zeros.
+inline int encode_b4d(CUtensorMap *map, const void *ptr, uint64_t N, uint64_t Kpr, uint64_t W,
+                      uint32_t atoms)
+{
+    EncodeTiled enc;
+    int rc = get_encoder(&enc);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    const cuuint64_t dims[4] = {64, Kpr, N / 64, W};
+    const cuuint64_t strides[3] = {N * 2, 128, Kpr * N * 2};
+    const cuuint32_t box[4] = {64, 64, atoms, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_RS_ERR_CUDA, "cuTensorMapEncodeTiled (4D B) failed (CUresult %d)", (int)r);
+    return GEMM_RS_OK;
+}
+
+// The B tensor map of a launch: 4D with one box per stage when N is a
+// multiple of 64 (atoms = the 64-column atoms a CTA loads per stage), else
+// 3D with one 64-column box per atom.  Returns the `b4d` kernel argument
+// through *b4d.
+inline int encode_b(CUtensorMap *map, const void *ptr, uint64_t N, uint64_t Kpr, uint64_t W,
+                    uint32_t atoms, int *b4d)
+{
+    if (N % 64 == 0) {
+        *b4d = 1;
+        return encode_b4d(map, ptr, N, Kpr, W, atoms);
+    }
+    *b4d = 0;
+    return encode_3d(map, ptr, N, Kpr, W, 64, 64);
+}
+
 } // namespace gemm_rs_host

@@ -272,6 +272,7 @@ struct gemm_rs_s {
     int reduce_mode; // GEMM_RS_REDUCE_* (default CHAIN)
     CUtensorMap tmA, tmB;
     const void *tmA_ptr, *tmB_ptr;
+    int tmB_atoms, tmB_4d; // the B map's atoms per load, and whether it is 4D
     unsigned long long timeout;
     int32_t *record;
     int debug_flags;
@@ -399,6 +400,8 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->rank_order = GEMM_RS_RANKS_DEFAULT;
     h->reduce_mode = GEMM_RS_REDUCE_CHAIN;
     h->tmA_ptr = h->tmB_ptr = nullptr;
+    h->tmB_atoms = 0;
+    h->tmB_4d = 0;
     h->timeout = 1ull << 32;
     h->record = nullptr;
     h->debug_flags = 0;
@@ -562,11 +565,16 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
                 return rc;
             h->tmA_ptr = A;
         }
-        if (B != h->tmB_ptr) {
-            // B: [W][K/W][N] -> dims {N, K/W, W}, box {64, 64, 1}
-            if ((rc = encode_3d(&h->tmB, B, h->N, h->Kpr, h->W, 64, gemm_rs::kBK)) != GEMM_RS_OK)
+        // B: [W][K/W][N] as 4D {64, K/W, N/64, W} with one box per stage (the
+        // CTA's 64-column atoms: BN/64, or 2 for a CTA of a 256-column pair
+        // tile), or as 3D {N, K/W, W} with 64x64 boxes when N % 64 != 0
+        const int atoms = h->bm == 2 * gemm_rs::kBM ? 2 : h->bn / 64;
+        if (B != h->tmB_ptr || atoms != h->tmB_atoms) {
+            h->tmB_ptr = nullptr;
+            if ((rc = encode_b(&h->tmB, B, h->N, h->Kpr, h->W, atoms, &h->tmB_4d)) != GEMM_RS_OK)
                 return rc;
             h->tmB_ptr = B;
+            h->tmB_atoms = atoms;
         }
     }
     int dev = 0;
@@ -609,6 +617,7 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.record = h->record;
     a.timeout = h->timeout;
     a.stall_producer = (h->debug_flags & GEMM_RS_DEBUG_STALL_PRODUCER) ? 1 : 0;
+    a.b4d = h->Kpr > 0 ? h->tmB_4d : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (h->bm == 2 * gemm_rs::kBM) {
@@ -837,8 +846,6 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
             return fail(GEMM_RS_ERR_ALIGN, "A and B must be 16-byte aligned");
         if ((rc = encode_3d(&tmA, A, Kpr, M, W, gemm_rs::kBK, gemm_rs::kBM)) != GEMM_RS_OK)
             return rc;
-        if ((rc = encode_3d(&tmB, B, N, Kpr, W, 64, gemm_rs::kBK)) != GEMM_RS_OK)
-            return rc;
     }
     int dev = 0, sms = 0;
     uint8_t *scratch = nullptr;
@@ -853,6 +860,9 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
         return cuda_fail(e, "cudaMemsetAsync(static scratch counters)");
 
     const int bn = pick_bn(M, N, W, sms);
+    int b4d = 0;
+    if (Kpr > 0 && (rc = encode_b(&tmB, B, N, Kpr, W, bn / 64, &b4d)) != GEMM_RS_OK)
+        return rc;
     gemm_rs::KernelArgs a{};
     a.W = W;
     a.M = static_cast<int>(M);
@@ -882,6 +892,7 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     a.record = nullptr;
     a.timeout = 1ull << 32;
     a.stall_producer = 0;
+    a.b4d = b4d;
     const int grid = static_cast<int>(a.total < sms ? a.total : sms);
     switch (bn) {
     case 256:

@@ -143,6 +143,7 @@ struct KernelArgs {
     int32_t *record;
     unsigned long long timeout;
     int stall_producer;
+    int b4d;        // 1: the B tensor map is 4D (one load per stage), 0: 3D (one per 64 columns)
 };
 
 struct SmemCtl {
@@ -265,10 +266,14 @@ __device__ __forceinline__ void run_producer(const KernelArgs &a, const Sched &s
                 ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
                 const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
                 ptx::tma_load_3d(sa, tmA, fb, kb * kBK, mt * kBM, r, pol);
+                if (a.b4d) {
+                    ptx::tma_load_4d(sa + Cfg::kABytes, tmB, fb, 0, kb * kBK, nt * (BN / 64), r, pol);
+                } else {
 #pragma unroll
-                for (int j = 0; j < BN / 64; ++j)
-                    ptx::tma_load_3d(sa + Cfg::kABytes + j * 8192, tmB, fb, nt * BN + j * 64,
-                                     kb * kBK, r, pol);
+                    for (int j = 0; j < BN / 64; ++j)
+                        ptx::tma_load_3d(sa + Cfg::kABytes + j * 8192, tmB, fb, nt * BN + j * 64,
+                                         kb * kBK, r, pol);
+                }
                 ++issued;
                 if (++stage == Cfg::kStages) {
                     stage = 0;
@@ -368,9 +373,11 @@ __device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// Write 8 consecutive output columns (m, n .. n+7) of Y in its dtype.
+// Write 8 consecutive output columns (m, n .. n+7) of Y in its dtype.  The
+// kernel never reads Y back, so its lines go first when L2 needs room (the
+// running sums and operands stay): `pol` is an evict-first policy.
 __device__ __forceinline__ void store_y8(const KernelArgs &a, int64_t m, int64_t n, float4 lo,
-                                         float4 hi)
+                                         float4 hi, uint64_t pol)
 {
 #ifdef GEMM_RS_CHECKED
     if (!in_mn(a, m, n))
@@ -378,8 +385,8 @@ __device__ __forceinline__ void store_y8(const KernelArgs &a, int64_t m, int64_t
 #endif
     if (a.y_fp32) {
         float *yp = static_cast<float *>(a.Y) + m * a.N + n;
-        ptx::st_f4(yp, lo);
-        ptx::st_f4(yp + 4, hi);
+        ptx::st_f4_hint(yp, lo, pol);
+        ptx::st_f4_hint(yp + 4, hi, pol);
     } else {
         const __nv_bfloat162 h0 = __floats2bfloat162_rn(lo.x, lo.y);
         const __nv_bfloat162 h1 = __floats2bfloat162_rn(lo.z, lo.w);
@@ -390,7 +397,7 @@ __device__ __forceinline__ void store_y8(const KernelArgs &a, int64_t m, int64_t
         w.y = *reinterpret_cast<const uint32_t *>(&h1);
         w.z = *reinterpret_cast<const uint32_t *>(&h2);
         w.w = *reinterpret_cast<const uint32_t *>(&h3);
-        ptx::st_u4(static_cast<uint16_t *>(a.Y) + m * a.N + n, w);
+        ptx::st_u4_hint(static_cast<uint16_t *>(a.Y) + m * a.N + n, w, pol);
     }
 }
 
@@ -436,6 +443,7 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
                 static_cast<int64_t>(q) * S * 1024;
     float *qb = q0 + static_cast<int64_t>(b) * Cfg::kSlotFloats; // slot b
     const int first = lo > b + 1 ? lo : b + 1;
+    const uint64_t y_pol = ptx::policy_evict_first();
 #pragma unroll 1
     for (int slab = slab0; slab < slab1; ++slab) {
         // One slab of a slot is 8 float4 per lane (a 4 KB block per warp),
@@ -483,7 +491,7 @@ __device__ __forceinline__ void fold_quarter(const KernelArgs &a, int tile, int 
             for (int j2 = 0; j2 < 4; ++j2) {
                 const int64_t n = static_cast<int64_t>(nt) * BN + slab * 32 + j2 * 8;
                 if (row_ok && n < a.N) // N is a multiple of 8
-                    store_y8(a, m, n, y[2 * j2], y[2 * j2 + 1]);
+                    store_y8(a, m, n, y[2 * j2], y[2 * j2 + 1], y_pol);
             }
         } else if (sb_ok) {
             float *dst = qb + slab * 1024 + lane * 4;
@@ -688,6 +696,7 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     // not let them push the B panels out of L2.  Chain-mode slots are read at
     // the next step: keep them.
     const uint64_t st_pol = a.chain ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+    const uint64_t y_pol = ptx::policy_evict_first();
     bool ok = true;
     uint32_t rq_n = 0;
     int it = 0;
@@ -875,7 +884,8 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
                     if (row_ok && n < a.N)
                         store_y8(a, m, n,
                                  make_float4(p[8 * g8], p[8 * g8 + 1], p[8 * g8 + 2], p[8 * g8 + 3]),
-                                 make_float4(p[8 * g8 + 4], p[8 * g8 + 5], p[8 * g8 + 6], p[8 * g8 + 7]));
+                                 make_float4(p[8 * g8 + 4], p[8 * g8 + 5], p[8 * g8 + 6], p[8 * g8 + 7]),
+                                 y_pol);
                 }
             } else if (add_l2) {
                 // running sum + this position's partial, added in L2
@@ -1133,10 +1143,17 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
                 const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
                 ptx::tma_load_3d_pair(sa, tmA, fb_leader, kb * kBK, mt2 * (2 * kBM) + crank * kBM, r,
                                       polA);
+                if (a.b4d) {
+                    ptx::tma_load_4d_pair(sa + Cfg::kABytes, tmB, fb_leader, 0, kb * kBK,
+                                          (nt * BN + static_cast<int>(crank) * (BN / 2)) / 64, r,
+                                          polB);
+                } else {
 #pragma unroll
-                for (int j = 0; j < BN / 128; ++j)
-                    ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
-                                          nt * BN + crank * (BN / 2) + j * 64, kb * kBK, r, polB);
+                    for (int j = 0; j < BN / 128; ++j)
+                        ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
+                                              nt * BN + crank * (BN / 2) + j * 64, kb * kBK, r,
+                                              polB);
+                }
                 ++issued;
                 if (++stage == Cfg::kStages) {
                     stage = 0;

@@ -109,6 +109,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// B as a 4D tensor {64, K/W, N/64, W}: one box {64, 64, atoms, 1} brings
+// `atoms` consecutive 64-column swizzle atoms of one k-block, each 64 rows x
+// 128 bytes, one after another in shared memory: the same layout as `atoms`
+// separate 3D boxes, in one instruction.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
 // L2 eviction-priority policies for the cache_hint operand.
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
@@ -305,6 +321,20 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// The 4D B load of a CTA pair (see tma_load_4d), completing on the even CTA's
+// barrier.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t cluster_bar, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -464,6 +494,14 @@ __device__ __forceinline__ void red_add_f4(float *p, float4 v)
 __device__ __forceinline__ void discard_l2_line(const void *p)
 {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// 16-byte store (raw bits) with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_u4_hint(void *p, uint4 v, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
 }
 
 // 16-byte read-only load (C, the bias-like epilogue input).

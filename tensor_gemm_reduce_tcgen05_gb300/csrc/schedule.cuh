@@ -53,65 +53,74 @@ struct Sched {
     int seq;      // 1: ranks one after another, 0: ranks side by side
 };
 
-__host__ __device__ __forceinline__ int64_t ceil_shift(int64_t x, int s)
-{
-    return (x + (int64_t(1) << s) - 1) >> s;
-}
-
 // Decode global entry g into (r, mt, nt) and the tile's position (0 .. W-1)
 // in its contributions' arrival order: the step in which rank r reaches the
 // tile's chunk (interleaved), or r (sequential).  g must be < W*nM*nN.
-__host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g, int &r, int &mt,
+//
+// Every quantity fits in 32 bits (the host bounds W*nM*nN below 2^31 and M
+// below 2^31), and the arithmetic is 32-bit: the producer decodes each tile
+// on its critical path, where 64-bit divisions cost about a microsecond.
+__host__ __device__ __forceinline__ void decode_tile(const Sched &s, int64_t g64, int &r, int &mt,
                                                      int &nt, int &pos)
 {
-    const int64_t G = s.G < s.nN ? s.G : s.nN;
+    const uint32_t g = static_cast<uint32_t>(g64);
+    const uint32_t W = static_cast<uint32_t>(s.W);
+    const uint32_t nM = static_cast<uint32_t>(s.nM);
+    const uint32_t nN = static_cast<uint32_t>(s.nN);
+    const uint32_t G = static_cast<uint32_t>(s.G) < nN ? static_cast<uint32_t>(s.G) : nN;
     // Every column group but the last is full, so the group index follows
     // directly.  p becomes rank r's index inside the group.
-    int64_t p, grp;
+    uint32_t p, grp, rr;
     if (s.seq) {
-        const int64_t full = static_cast<int64_t>(s.W) * s.nM * G; // entries of a full group
+        const uint32_t full = W * nM * G; // entries of a full group
         grp = g / full;
-        const int64_t gn = (s.nN - grp * G) < G ? (s.nN - grp * G) : G;
-        const int64_t q = g - grp * full;
-        const int64_t per_rank = static_cast<int64_t>(s.nM) * gn;
-        r = static_cast<int>(q / per_rank);
-        p = q - static_cast<int64_t>(r) * per_rank;
+        const uint32_t gn = (nN - grp * G) < G ? (nN - grp * G) : G;
+        const uint32_t q = g - grp * full;
+        const uint32_t per_rank = nM * gn;
+        rr = q / per_rank;
+        p = q - rr * per_rank;
     } else {
-        r = static_cast<int>(g % s.W);
-        p = g / s.W;
-        grp = p / (G * s.nM);
-        p -= grp * G * s.nM;
+        rr = g % W;
+        p = g / W;
+        grp = p / (G * nM);
+        p -= grp * G * nM;
     }
-    const int64_t g0 = grp * G;
-    const int64_t gn = (s.nN - g0) < G ? (s.nN - g0) : G;
-    const int64_t rot = (static_cast<int64_t>((s.W - r) % s.W) * gn) / s.W;
-    for (int st = 0; st < s.W; ++st) {
-        int c = r + 1 + st;
-        if (c >= s.W)
-            c -= s.W;
-        if (c >= s.W)
-            c -= s.W;
-        // row tiles whose first row lies in chunk c: [ceil(c*R/BM), ceil((c+1)*R/BM))
-        const int64_t first = ceil_shift(static_cast<int64_t>(c) * s.R, s.bm_shift);
-        const int64_t last = ceil_shift(static_cast<int64_t>(c + 1) * s.R, s.bm_shift);
-        const int64_t cnt = last - first;
-        const int64_t items = cnt * gn;
-        const int64_t RG = s.RG < cnt ? s.RG : cnt;
+    r = static_cast<int>(rr);
+    const uint32_t g0 = grp * G;
+    const uint32_t gn = (nN - g0) < G ? (nN - g0) : G;
+    const uint32_t rot = (((W - rr) % W) * gn) / W;
+    const uint32_t R = static_cast<uint32_t>(s.R);
+    const uint32_t bmask = (1u << s.bm_shift) - 1u;
+    // Step st visits chunk c = (r+1+st) mod W, whose row tiles are the ones
+    // whose first row lies in the chunk: [ceil(c*R/BM), ceil((c+1)*R/BM)).
+    uint32_t c = rr + 1 >= W ? rr + 1 - W : rr + 1;
+    uint32_t first = (c * R + bmask) >> s.bm_shift;
+    for (uint32_t st = 0; st < W; ++st) {
+        const uint32_t last = ((c + 1) * R + bmask) >> s.bm_shift;
+        const uint32_t cnt = last - first;
+        const uint32_t items = cnt * gn;
         if (p < items) {
             // Every row group but the chunk's last is full.
-            const int64_t rg = p / (RG * gn);
-            const int64_t q = p - rg * RG * gn;
-            const int64_t rn = (cnt - rg * RG) < RG ? (cnt - rg * RG) : RG;
-            const int64_t jl = q / rn;
+            const uint32_t RG = static_cast<uint32_t>(s.RG) < cnt ? static_cast<uint32_t>(s.RG) : cnt;
+            const uint32_t rg = p / (RG * gn);
+            const uint32_t q = p - rg * RG * gn;
+            const uint32_t rn = (cnt - rg * RG) < RG ? (cnt - rg * RG) : RG;
+            const uint32_t jl = q / rn;
             mt = static_cast<int>(first + rg * RG + (q - jl * rn));
-            int64_t n = jl + rot;
+            uint32_t n = jl + rot;
             if (n >= gn)
                 n -= gn;
             nt = static_cast<int>(g0 + n);
-            pos = s.seq ? r : st;
+            pos = s.seq ? static_cast<int>(rr) : static_cast<int>(st);
             return;
         }
         p -= items;
+        if (++c == W) {
+            c = 0;
+            first = 0;
+        } else {
+            first = last;
+        }
     }
     mt = -1;
     nt = -1;
