@@ -192,24 +192,9 @@ __device__ __forceinline__ void run_ag_producer(const AgArgs &g, const KernelArg
             }
         }
     }
-    if (!ok) {
+    if (!ok)
         report(ka, ctl, kStatusTimeoutProducer);
-        if (crank == 0) {
-            const int64_t n = issued < Cfg::kStages ? issued : Cfg::kStages;
-            for (int64_t i = 1; i <= n; ++i) {
-                const int64_t pos = issued - i;
-                const uint32_t s = static_cast<uint32_t>(pos % Cfg::kStages);
-                const uint32_t ph = static_cast<uint32_t>((pos / Cfg::kStages) & 1);
-                ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->full[s]), ph, g.timeout, nullptr);
-            }
-        } else {
-            // The odd CTA cannot observe its loads on the even CTA's barrier:
-            // give any load in flight time to land before the pair tears down.
-            const unsigned long long t0 = clock64();
-            while (clock64() - t0 < (1ull << 20)) {
-            }
-        }
-    }
+    pair_producer_finish(ctl, crank, ok, issued, Cfg::kStages, g.timeout);
 }
 
 // Epilogue (warps 2-5): H_r[m, n] = alpha * acc, 32 columns per step.
@@ -362,6 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&ctl->acc_empty[b]), 8); // 4 epilogue warps x 2 CTAs
         }
         ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+        ptx::mbar_init(ptx::smem_u32(&ctl->peer_drained), 1);
         ctl->abort = 0;
         ptx::fence_barrier_init();
     }

@@ -154,6 +154,7 @@ struct SmemCtl {
     uint64_t rq_full[kRQ];
     uint64_t rq_empty[kRQ];
     uint64_t drain;
+    uint64_t peer_drained; // CTA pairs: the odd CTA's loads have landed (the even CTA arrives)
     int32_t rq_tile[kRQ];
     uint32_t rq_head; // next queue entry to claim
     int epi_direct[2]; // chain mode: the epilogue owns the fold of the tile in TMEM buffer b
@@ -1102,6 +1103,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ CTA-pair kernel
+// End of a pair producer.  Both CTAs' loads complete on the even CTA's `full`
+// barriers, so only the even CTA can see them land.  After a failure the even
+// CTA waits (bounded) for its last fills of every stage; after a normal run
+// its tail has already waited for every stage to be released, which follows
+// the stage's loads.  Either way it then arrives on the odd CTA's
+// `peer_drained` barrier.  The odd CTA, after a failure of its own, waits on
+// that barrier (bounded) before the pair tears down, so it never leaves with
+// one of its loads still writing into its shared memory.
+__device__ __forceinline__ void pair_producer_finish(SmemCtl *ctl, uint32_t crank, bool ok,
+                                                     int64_t issued, int stages,
+                                                     unsigned long long timeout)
+{
+    if (crank == 0) {
+        if (!ok) {
+            const int64_t n = issued < stages ? issued : stages;
+            for (int64_t i = 1; i <= n; ++i) {
+                const int64_t pos = issued - i;
+                const uint32_t s = static_cast<uint32_t>(pos % stages);
+                const uint32_t ph = static_cast<uint32_t>((pos / stages) & 1);
+                ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->full[s]), ph, timeout, nullptr);
+            }
+        }
+        ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&ctl->peer_drained), 1));
+    } else if (!ok) {
+        ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->peer_drained), 0u, timeout, nullptr);
+    }
+}
+
 // Producer of one CTA of a pair.  Both CTAs load into their own shared memory.
 // The loads count their bytes on the even CTA's `full` barrier, which only the
 // even CTA arms (expect_tx of both CTAs' bytes).
@@ -1177,26 +1206,9 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
             }
         }
     }
-    if (!ok) {
+    if (!ok)
         report(a, ctl, kStatusTimeoutProducer);
-        if (crank == 0) {
-            // The even CTA's `full` barriers count both CTAs' bytes.
-            const int64_t n = issued < Cfg::kStages ? issued : Cfg::kStages;
-            for (int64_t i = 1; i <= n; ++i) {
-                const int64_t pos = issued - i;
-                const uint32_t s = static_cast<uint32_t>(pos % Cfg::kStages);
-                const uint32_t ph = static_cast<uint32_t>((pos / Cfg::kStages) & 1);
-                ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->full[s]), ph, a.timeout, nullptr);
-            }
-        } else {
-            // The odd CTA cannot observe its loads on the even CTA's barrier:
-            // give any load still in flight time to land (2^20 cycles) before
-            // the CTA pair tears down.
-            const unsigned long long t0 = clock64();
-            while (clock64() - t0 < (1ull << 20)) {
-            }
-        }
-    }
+    pair_producer_finish(ctl, crank, ok, issued, Cfg::kStages, a.timeout);
 }
 
 // MMA issuer of the pair (one thread of the even CTA).
@@ -1294,6 +1306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&ctl->rq_empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&ctl->drain), 1);
+        ptx::mbar_init(ptx::smem_u32(&ctl->peer_drained), 1);
         ctl->abort = 0;
         ctl->rq_head = 0;
         ptx::fence_barrier_init();
