@@ -347,24 +347,47 @@ GEMM_RS_API int gemm_rs_reduce_partials(const void *partials, gemm_rs_dtype part
  *   A, B, C, Y                         as for gemm_rs_run (device, 16-byte aligned).
  *   stream                             the call is asynchronous on this stream.
  *
- * - The first call on a device does a one-time set-up on that device: kernel
- *   attributes, plus a cudaGetSymbolAddress lookup of the scratch array.  Make
- *   that first call before any stream capture begins.
+ * - The first call in a context does a one-time set-up there (kernel
+ *   attributes).  Every call looks up the scratch array's device address with
+ *   cudaGetSymbolAddress (no allocation).  Make the first call before any
+ *   stream capture begins.
  * - Each call clears the status word and the tile counters with one
  *   cudaMemsetAsync on `stream`.  The scratch keeps the previous call's
  *   contents otherwise.
  * - Every call on a device shares the one scratch array.  Calls that overlap
  *   on the GPU (different streams, or host threads with no ordering between
  *   them) race on it and give wrong results.  Order them on one stream.
+ * - The scratch address is looked up on every call, in the calling thread's
+ *   current CUDA context, so callers that own several contexts on one device
+ *   get the array of the context they run in.  The kernel attributes are set
+ *   once per context.
  * - A shape whose gemm_rs_workspace_bytes exceeds GEMM_RS_NOALLOC_SCRATCH_BYTES
  *   is rejected with GEMM_RS_ERR_WORKSPACE.  Other errors are as for
- *   gemm_rs_create and gemm_rs_run.  Device-side timeouts are not reported:
- *   use a handle (gemm_rs_status) when that is needed.
+ *   gemm_rs_create and gemm_rs_run.  A device-side timeout leaves its code in
+ *   the scratch's status word until the next call clears it: read it with
+ *   gemm_rs_noalloc_status before the next call.
  */
 GEMM_RS_API int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float alpha,
                                     float beta, gemm_rs_dtype y_dtype, const void *A,
                                     const void *B, const void *C, void *Y,
                                     gemm_rs_stream_t stream);
+
+/*
+ * GEMM_RS_NOALLOC_SCRATCH_BYTES as compiled into this library (the size of its
+ * static scratch), for callers and bindings that do not read this header.
+ */
+GEMM_RS_API size_t gemm_rs_noalloc_scratch_bytes(void);
+
+/*
+ * The outcome of the last gemm_rs_run_noalloc call in the current context, for
+ * callers without a handle.  Waits for `stream` (the stream of that call),
+ * reads the status word of the static scratch, and clears it.  Allocates
+ * nothing (the word is copied into a host variable).  Returns GEMM_RS_OK,
+ * GEMM_RS_ERR_TIMEOUT (a device wait ran out; Y is not valid),
+ * GEMM_RS_ERR_BOUNDS (checked build only) or GEMM_RS_ERR_CUDA.  The next
+ * gemm_rs_run_noalloc clears the word too, so call this in between.
+ */
+GEMM_RS_API int gemm_rs_noalloc_status(gemm_rs_stream_t stream);
 
 /* Library version string. */
 GEMM_RS_API const char *gemm_rs_version(void);

@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_reduce_partials": (i32, [vp, i32, vp, vp, i64, i64, i32, f32, f32, i32, vp]),
             "gemm_rs_version": (ctypes.c_char_p, []),
             "gemm_rs_run_noalloc": (i32, [i64, i64, i64, i32, f32, f32, i32, vp, vp, vp, vp, vp]),
+            "gemm_rs_noalloc_scratch_bytes": (sz, []),
+            "gemm_rs_noalloc_status": (i32, [vp]),
             "ag_gemm_workspace_bytes": (sz, [i64, i64, i64, i32]),
             "ag_gemm_create": (i32, [ctypes.POINTER(vp), i64, i64, i64, i32, f32, i32, vp, sz, vp]),
             "ag_gemm_run": (i32, [vp, vp, vp, vp, vp]),
@@ -218,7 +220,15 @@ def gemm_rs_run_noalloc(M, N, K, W, alpha, beta, y_dtype, A, B, C, Y, stream=0) 
     _check(lib().gemm_rs_run_noalloc(M, N, K, W, alpha, beta, y_dtype, A, B, C, Y, stream))
 
 
-GEMM_RS_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+def gemm_rs_noalloc_scratch_bytes() -> int:
+    """The size of gemm_rs_run_noalloc's static scratch, as compiled into the library."""
+    return int(lib().gemm_rs_noalloc_scratch_bytes())
+
+
+def gemm_rs_noalloc_status(stream=0) -> int:
+    """Read and clear the status word of the static scratch (after waiting for
+    `stream`): 0, or raises GemmRSError for a device timeout."""
+    return _check(lib().gemm_rs_noalloc_status(stream))
 
 
 def _cuda_device(device):

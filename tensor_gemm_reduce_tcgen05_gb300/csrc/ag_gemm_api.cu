@@ -60,49 +60,53 @@ int ag_slice_rows(int64_t K)
 }
 
 struct AgDevice {
+    int dev = 0;
     int clusters = 0;
-    bool ready = false;
 };
-AgDevice g_ag_dev[64];
-std::mutex g_ag_mu;
+ContextCache<AgDevice> g_ag_dev;
 
-int ag_prepare(int *dev_out, int *clusters_out)
+// Once per CUDA context: check the device, set the kernel's shared-memory
+// attribute and count the co-resident CTA pairs.
+int ag_setup(AgDevice &d)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64)
-        return fail(GEMM_RS_ERR_ARG, "device index %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_ag_mu);
-    AgDevice &d = g_ag_dev[dev];
-    if (!d.ready) {
-        int major = 0, minor = 0;
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-        if (major != 10 || minor != 3)
-            return fail(GEMM_RS_ERR_UNSUPPORTED,
-                        "device %d has compute capability %d.%d; this library is built for sm_103a", dev,
-                        major, minor);
-        int sms = 0;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-        if ((e = cudaFuncSetAttribute(gemm_rs::ag_gemm_pair_kernel<256>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      gemm_rs::smem_bytes_pair<256>())) != cudaSuccess)
-            return cuda_fail(e, "cudaFuncSetAttribute(AG kernel shared memory)");
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-        cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = gemm_rs::smem_bytes_pair<256>();
-        int clusters = 0;
-        if ((e = cudaOccupancyMaxActiveClusters(&clusters, gemm_rs::ag_gemm_pair_kernel<256>, &cfg)) !=
-            cudaSuccess)
-            return cuda_fail(e, "cudaOccupancyMaxActiveClusters(AG kernel)");
-        d.clusters = clusters > 0 ? clusters : 1;
-        d.ready = true;
-    }
-    *dev_out = dev;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(GEMM_RS_ERR_UNSUPPORTED,
+                    "device %d has compute capability %d.%d; this library is built for sm_103a", dev,
+                    major, minor);
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaFuncSetAttribute(gemm_rs::ag_gemm_pair_kernel<256>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  gemm_rs::smem_bytes_pair<256>())) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(AG kernel shared memory)");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = gemm_rs::smem_bytes_pair<256>();
+    int clusters = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&clusters, gemm_rs::ag_gemm_pair_kernel<256>, &cfg)) !=
+        cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters(AG kernel)");
+    d.dev = dev;
+    d.clusters = clusters > 0 ? clusters : 1;
+    return GEMM_RS_OK;
+}
+
+int ag_prepare(int *dev_out, int *clusters_out)
+{
+    AgDevice d;
+    const int rc = g_ag_dev.get(&d, ag_setup);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    *dev_out = d.dev;
     *clusters_out = d.clusters;
     return GEMM_RS_OK;
 }

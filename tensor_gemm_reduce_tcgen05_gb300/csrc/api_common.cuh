@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 #include <string>
 
 #include "gemm_rs.h"
@@ -61,6 +62,70 @@ inline int get_encoder(EncodeTiled *out)
     *out = fn;
     return GEMM_RS_OK;
 }
+
+// The calling thread's current CUDA context (a driver handle), for caches of
+// per-context set-up.  cuCtxGetCurrent comes from the driver, looked up once.
+inline int current_context(void **out)
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    static GetCurrent fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+            return fail(GEMM_RS_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+        fn = reinterpret_cast<GetCurrent>(p);
+    }
+    CUcontext ctx = nullptr;
+    const CUresult r = fn(&ctx);
+    if (r != CUDA_SUCCESS || ctx == nullptr)
+        return fail(GEMM_RS_ERR_CUDA, "no current CUDA context (CUresult %d)", (int)r);
+    *out = ctx;
+    return GEMM_RS_OK;
+}
+
+// Per-context set-up (kernel attributes, occupancy), keyed by the driver's
+// context handle: a host application may run several contexts on one device,
+// and each needs the kernels' attributes set in it.  A small table; when it
+// is full the oldest entry is replaced.  Lookups hold the table's mutex.
+template <typename T>
+struct ContextCache {
+    static constexpr int kEntries = 32;
+    struct Entry {
+        void *ctx = nullptr;
+        T info{};
+    };
+    Entry e[kEntries];
+    int next = 0;
+    std::mutex mu;
+
+    // The entry of the current context, set up by setup(T&) (an int-returning
+    // callable) the first time; its return code is passed on.
+    template <typename F>
+    int get(T *out, F setup)
+    {
+        void *ctx = nullptr;
+        int rc = current_context(&ctx);
+        if (rc != GEMM_RS_OK)
+            return rc;
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < kEntries; ++i)
+            if (e[i].ctx == ctx) {
+                *out = e[i].info;
+                return GEMM_RS_OK;
+            }
+        T info{};
+        if ((rc = setup(info)) != GEMM_RS_OK)
+            return rc;
+        e[next].ctx = ctx;
+        e[next].info = info;
+        next = (next + 1) % kEntries;
+        *out = info;
+        return GEMM_RS_OK;
+    }
+};
 
 // 3-D bf16 tensor map {d0, d1, d2} (d0 contiguous), box {b0, b1, 1}, 128-byte
 // swizzle, zero fill outside the tensor.

@@ -70,12 +70,11 @@ int check_shape(int64_t M, int64_t N, int64_t K, int W)
 }
 
 struct DeviceInfo {
+    int dev = 0;
     int sms = 0;
     int pair_clusters = 0; // CTA pairs of the pair kernel that fit on the device at once
-    bool attrs_set = false;
 };
-constexpr int kMaxDevices = 64;
-DeviceInfo g_dev[kMaxDevices];
+ContextCache<DeviceInfo> g_dev;
 
 template <int BN>
 cudaError_t set_kernel_attrs()
@@ -92,47 +91,64 @@ cudaError_t set_pair_kernel_attrs()
                                 gemm_rs::smem_bytes_pair<256>());
 }
 
-int prepare_device(int *dev_out, int *sms_out, int *pair_clusters_out = nullptr)
+// Once per CUDA context: check the device, set the kernels' shared-memory
+// attributes and count the co-resident CTA pairs.
+int setup_device(DeviceInfo &d)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices)
-        return fail(GEMM_RS_ERR_UNSUPPORTED, "device index %d out of range", dev);
-    DeviceInfo &d = g_dev[dev];
-    if (!d.attrs_set) {
-        int major = 0, minor = 0;
-        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute(major)");
-        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
-        if (major != 10 || minor != 3)
-            return fail(GEMM_RS_ERR_UNSUPPORTED,
-                        "device %d has compute capability %d.%d; this library is built for sm_103a",
-                        dev, major, minor);
-        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-        if ((e = set_kernel_attrs<256>()) != cudaSuccess ||
-            (e = set_kernel_attrs<128>()) != cudaSuccess ||
-            (e = set_kernel_attrs<64>()) != cudaSuccess || (e = set_pair_kernel_attrs()) != cudaSuccess)
-            return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
-        cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = gemm_rs::smem_bytes_pair<256>();
-        int clusters = 0;
-        if ((e = cudaOccupancyMaxActiveClusters(&clusters, gemm_rs::gemm_rs_pair_kernel<256>, &cfg)) !=
-            cudaSuccess)
-            return cuda_fail(e, "cudaOccupancyMaxActiveClusters(pair kernel)");
-        d.pair_clusters = clusters > 0 ? clusters : 1;
-        d.attrs_set = true;
-    }
-    *dev_out = dev;
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute(major)");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute(minor)");
+    if (major != 10 || minor != 3)
+        return fail(GEMM_RS_ERR_UNSUPPORTED,
+                    "device %d has compute capability %d.%d; this library is built for sm_103a",
+                    dev, major, minor);
+    d.dev = dev;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = set_kernel_attrs<256>()) != cudaSuccess ||
+        (e = set_kernel_attrs<128>()) != cudaSuccess ||
+        (e = set_kernel_attrs<64>()) != cudaSuccess || (e = set_pair_kernel_attrs()) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
+    cfg.blockDim = dim3(gemm_rs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = gemm_rs::smem_bytes_pair<256>();
+    int clusters = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&clusters, gemm_rs::gemm_rs_pair_kernel<256>, &cfg)) !=
+        cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters(pair kernel)");
+    d.pair_clusters = clusters > 0 ? clusters : 1;
+    return GEMM_RS_OK;
+}
+
+int prepare_device(int *dev_out, int *sms_out, int *pair_clusters_out = nullptr)
+{
+    DeviceInfo d;
+    const int rc = g_dev.get(&d, setup_device);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    *dev_out = d.dev;
     *sms_out = d.sms;
     if (pair_clusters_out)
         *pair_clusters_out = d.pair_clusters;
     return GEMM_RS_OK;
+}
+
+// The error a non-zero status word reports (the word is then cleared by the caller).
+int status_word_error(uint32_t word)
+{
+    if (word == gemm_rs::kStatusOutOfBounds)
+        return fail(GEMM_RS_ERR_BOUNDS,
+                    "checked build: an access outside its buffer was caught and skipped");
+    static const char *role[] = {"?", "TMA producer", "MMA issuer", "epilogue", "reducer"};
+    return fail(GEMM_RS_ERR_TIMEOUT, "device wait timed out in the %s (status %u)",
+                role[word < 5 ? word : 0], word);
 }
 
 int stages_for(int bm, int bn)
@@ -667,12 +683,7 @@ int gemm_rs_status(gemm_rs_t h, gemm_rs_stream_t stream)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(e, "clearing the status word");
-    if (word == gemm_rs::kStatusOutOfBounds)
-        return fail(GEMM_RS_ERR_BOUNDS,
-                    "checked build: an access outside its buffer was caught and skipped");
-    static const char *role[] = {"?", "TMA producer", "MMA issuer", "epilogue", "reducer"};
-    return fail(GEMM_RS_ERR_TIMEOUT, "device wait timed out in the %s (status %u)",
-                role[word < 5 ? word : 0], word);
+    return status_word_error(word);
 }
 
 int gemm_rs_reset(gemm_rs_t h, gemm_rs_stream_t stream)
@@ -773,37 +784,25 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(GEMM_RS_NOALLOC_SCRATCH_BYTES);
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct NoAllocDevice {
-    uint8_t *scratch = nullptr; // device address of g_noalloc_scratch on this device
-    int sms = 0;
-};
-NoAllocDevice g_noalloc_dev[kMaxDevices];
-std::mutex g_noalloc_mutex;
-
-// Once per device, with that device current: kernel attributes and the device address of
-// the scratch array.  In host code the array's name is only a host-side stand-in, so
-// the address must come from cudaGetSymbolAddress.
+// With the current context's set-up done: the device address of g_noalloc_scratch
+// in that context.  In host code the array's name is only a host-side stand-in,
+// so the address comes from cudaGetSymbolAddress, looked up on every call (it
+// allocates nothing, and a cached address could belong to another context).
 int noalloc_device(int *dev_out, uint8_t **scratch_out, int *sms_out)
 {
     int dev = 0, sms = 0;
     int rc = prepare_device(&dev, &sms);
     if (rc != GEMM_RS_OK)
         return rc;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    NoAllocDevice &d = g_noalloc_dev[dev];
-    if (d.scratch == nullptr) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-        if (!aligned(p, 256))
-            return fail(GEMM_RS_ERR_ALIGN, "static scratch is not 256-byte aligned");
-        d.scratch = static_cast<uint8_t *>(p);
-        d.sms = sms;
-    }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    if (!aligned(p, 256))
+        return fail(GEMM_RS_ERR_ALIGN, "static scratch is not 256-byte aligned");
     *dev_out = dev;
-    *scratch_out = d.scratch;
-    *sms_out = d.sms;
+    *scratch_out = static_cast<uint8_t *>(p);
+    *sms_out = sms;
     return GEMM_RS_OK;
 }
 
@@ -912,4 +911,30 @@ extern "C" int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, float
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused GEMM+RS kernel (no-alloc entry point)");
     return GEMM_RS_OK;
+}
+
+extern "C" size_t gemm_rs_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int gemm_rs_noalloc_status(gemm_rs_stream_t stream)
+{
+    int dev = 0, sms = 0;
+    uint8_t *scratch = nullptr;
+    int rc = noalloc_device(&dev, &scratch, &sms);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the static scratch's status word");
+    if (word == 0)
+        return GEMM_RS_OK;
+    e = cudaMemsetAsync(scratch, 0, sizeof word, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "clearing the static scratch's status word");
+    return status_word_error(word);
 }

@@ -63,6 +63,16 @@ def test_no_torch_types_in_header(path):
     assert "at::" not in text and "c10" not in text
 
 
+def test_noalloc_scratch_size_is_the_headers(b):
+    """The static scratch's size comes from the library and equals the header's
+    GEMM_RS_NOALLOC_SCRATCH_BYTES (read without touching a device)."""
+    text = open(HEADER).read()
+    m = re.search(r"#define GEMM_RS_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", text)
+    assert m, "the header defines the scratch size"
+    want = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+    assert b.gemm_rs_noalloc_scratch_bytes() == want
+
+
 def test_version(b):
     assert "sm_103a" in b.gemm_rs_version()
 

@@ -83,6 +83,26 @@ for mode in (0, 1, 2):
     del Y, op
     torch.cuda.empty_cache()
 print("checked big ok")
+# the entry point that allocates nothing: its static scratch, every access checked
+na_cases = 0
+for (W, M, N, Kpr, beta, y_dtype) in [(4, 512, 520, 200, 1.0, "bf16"), (8, 64, 1024, 192, 0.0, "fp32"),
+                                     (3, 300, 520, 64, 0.5, "fp32")]:
+    A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int" if beta != 0 else None)
+    ref = oracle_y(A, B, C if beta != 0 else None, 1.0, beta, y_dtype)
+    code = b.GEMM_RS_BF16 if y_dtype == "bf16" else b.GEMM_RS_FP32
+    Ad, Bd = A.cuda(), B.cuda()
+    Cd = C.cuda() if beta != 0 else None
+    for _ in range(2):
+        Y = torch.empty((M, N), dtype=torch.bfloat16 if y_dtype == "bf16" else torch.float32,
+                        device="cuda:0")
+        Y.view(torch.uint8).fill_(0xFF)
+        b.gemm_rs_run_noalloc(M, N, W * Kpr, W, 1.0, beta, code, Ad.data_ptr(), Bd.data_ptr(),
+                              0 if Cd is None else Cd.data_ptr(), Y.data_ptr(), 0)
+        torch.cuda.synchronize()
+        assert b.gemm_rs_noalloc_status(0) == 0
+        np.testing.assert_array_equal(to_np_y(Y), ref)
+    na_cases += 1
+print("checked noalloc cases", na_cases)
 """
 
 
@@ -95,6 +115,7 @@ def test_checked_build_finds_no_access_out_of_bounds():
     assert "checked cases 144" in r.stdout
     assert "checked ag cases 12" in r.stdout
     assert "checked big ok" in r.stdout
+    assert "checked noalloc cases 3" in r.stdout
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])

@@ -8,7 +8,10 @@ scratch in a static device array of a fixed size.  This test calls it
 through the C ABI, twice in a row, and checks each output against the
 handle-based entry point (gemm_rs_create + gemm_rs_run) on the same inputs,
 within the tolerances the other parity tests use.  Both paths run the same
-kernel, so the outputs are also expected to match bit for bit.
+kernel, so the outputs are also expected to match bit for bit.  It also checks
+the claim in the name: once the first call has done its set-up, further calls
+leave torch's allocator and the device's free memory where they were, and the
+status query (which reads the scratch's status word) reports success.
 
 This file is collected last on purpose.  It must pass both on its own in a
 fresh process and after every other test.
@@ -40,7 +43,7 @@ def test_noalloc_matches_handle_path_on_two_calls_in_a_row(W, M, N, Kpr, alpha, 
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = None if C is None else C.to(dev)
     K = W * Kpr
-    assert b.gemm_rs_workspace_bytes(M, N, K, W) <= b.GEMM_RS_NOALLOC_SCRATCH_BYTES
+    assert b.gemm_rs_workspace_bytes(M, N, K, W) <= b.gemm_rs_noalloc_scratch_bytes()
 
     op = b.GemmRS(M, N, K, W, alpha, beta, y_dtype, device=dev)
     ref = to_np_y(op.run(Ad, Bd, Cd))
@@ -49,10 +52,22 @@ def test_noalloc_matches_handle_path_on_two_calls_in_a_row(W, M, N, Kpr, alpha, 
 
     code = b.GEMM_RS_BF16 if y_dtype == "bf16" else b.GEMM_RS_FP32
     stream = torch.cuda.current_stream(dev).cuda_stream
+    Ys = [_y(M, N, y_dtype) for _ in range(2)]
+    torch.cuda.synchronize()
     for call in range(2):
-        Y = _y(M, N, y_dtype)
+        Y = Ys[call]
+        if call == 1:
+            # the first call did the set-up; from here on nothing may allocate
+            torch.cuda.synchronize()
+            torch_before = (torch.cuda.memory_allocated(dev), torch.cuda.memory_reserved(dev))
+            free_before = torch.cuda.mem_get_info(dev)[0]
         b.gemm_rs_run_noalloc(M, N, K, W, alpha, beta, code, Ad.data_ptr(), Bd.data_ptr(),
                               0 if Cd is None else Cd.data_ptr(), Y.data_ptr(), stream)
+        assert b.gemm_rs_noalloc_status(stream) == b.GEMM_RS_OK
+        if call == 1:
+            assert (torch.cuda.memory_allocated(dev), torch.cuda.memory_reserved(dev)) == torch_before
+            # cudaMemGetInfo: no device allocation behind torch's back either
+            assert torch.cuda.mem_get_info(dev)[0] >= free_before - (1 << 20)
         torch.cuda.synchronize()
         y = to_np_y(Y)
         assert_close(y, ref, y_dtype, f"no-alloc call {call}")
@@ -62,7 +77,7 @@ def test_noalloc_matches_handle_path_on_two_calls_in_a_row(W, M, N, Kpr, alpha, 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     from tensor_gemm_reduce_tcgen05_gb300 import binding as b
     W, M, N, K = 8, 4096, 4096, 8 * 64
-    assert b.gemm_rs_workspace_bytes(M, N, K, W) > b.GEMM_RS_NOALLOC_SCRATCH_BYTES
+    assert b.gemm_rs_workspace_bytes(M, N, K, W) > b.gemm_rs_noalloc_scratch_bytes()
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda:0")
     A = torch.zeros((W, M, K // W), dtype=torch.bfloat16, device="cuda:0")
     B = torch.zeros((W, K // W, N), dtype=torch.bfloat16, device="cuda:0")
