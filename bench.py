@@ -49,6 +49,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused GEMM+RS TFLOP/s and % of GB300 bf16 tensor peak vs unfused, 1 GPU"
+# gemm_rs_set_reduce_mode codes (include/gemm_rs.h)
+REDUCE_MODES = {"chain": 0, "last_arriver": 1, "two_level": 2}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024  # written between calls to push earlier data out of L2
@@ -532,6 +534,8 @@ def run_ours(args):
     op = binding.GemmRS(w.M, w.N, w.K, w.W, w.alpha, w.beta, w.y_dtype, device=dev)
     if args.tile_n:
         binding.gemm_rs_set_tile_n(op.handle, args.tile_n)
+    if args.reduce_mode:
+        binding.gemm_rs_set_reduce_mode(op.handle, REDUCE_MODES[args.reduce_mode])
     Y = op.new_output()
     Y_pin = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
     if args.unfused_only:
@@ -1093,6 +1097,9 @@ def main(argv=None):
                     help="gemm_rs: the fused GEMM + reduce-scatter (the default line); "
                          "ag: the fused all-gather + GEMM; ffn: both, chained")
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--reduce-mode", choices=sorted(REDUCE_MODES), default=None,
+                    help="run the fused kernel in this reduction instead of the library's "
+                         "default (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sustain-seconds", type=float, default=None,
                     help="after the timed steps, run the same calls back to back for at least "
