@@ -46,6 +46,9 @@ int ag_check_shape(int64_t M, int64_t N, int64_t K, int W)
                     (long long)M, kAgTile * W);
     if (K % 8 != 0 || N % 8 != 0)
         return fail(GEMM_RS_ERR_SHAPE, "K and N must be multiples of 8 (16-byte TMA rows)");
+    // the kernel decodes its work items in 32-bit arithmetic
+    if (static_cast<int64_t>(W) * (M / kAgTile) * ((N + kAgTile - 1) / kAgTile) >= (int64_t(1) << 31))
+        return fail(GEMM_RS_ERR_SHAPE, "more than 2^31 work items");
     return GEMM_RS_OK;
 }
 
@@ -125,6 +128,7 @@ struct ag_gemm_s {
     uint32_t epoch;
     CUtensorMap tmX, tmG, tmB;
     const void *tmX_ptr, *tmB_ptr;
+    int tmB_4d; // B1's map is 4D (N % 64 == 0)
     unsigned long long timeout;
     int32_t *record;
     int debug_flags;
@@ -184,6 +188,7 @@ int ag_gemm_create(ag_gemm_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->nslices = static_cast<int>(M / W / h->slice_rows);
     h->epoch = 0;
     h->tmX_ptr = h->tmB_ptr = nullptr;
+    h->tmB_4d = 0;
     h->timeout = 1ull << 32;
     h->record = nullptr;
     h->debug_flags = 0;
@@ -221,9 +226,12 @@ int ag_gemm_run(ag_gemm_t h, const void *X, const void *B1, void *H, gemm_rs_str
         h->tmX_ptr = X;
     }
     if (B1 != h->tmB_ptr) {
-        // B1: [W][K][N] -> {N, K, W}, box {64, 64, 1}
-        if ((rc = encode_3d(&h->tmB, B1, static_cast<uint64_t>(h->N), static_cast<uint64_t>(h->K),
-                            static_cast<uint64_t>(h->W), 64, gemm_rs::kBK)) != GEMM_RS_OK)
+        // B1: [W][K][N] as 4D {64, K, N/64, W} with one box of a CTA's two
+        // 64-column atoms per stage, or 3D {N, K, W} with 64x64 boxes when
+        // N % 64 != 0
+        h->tmB_ptr = nullptr;
+        if ((rc = encode_b(&h->tmB, B1, static_cast<uint64_t>(h->N), static_cast<uint64_t>(h->K),
+                           static_cast<uint64_t>(h->W), 2, &h->tmB_4d)) != GEMM_RS_OK)
             return rc;
         h->tmB_ptr = B1;
     }
@@ -252,6 +260,7 @@ int ag_gemm_run(ag_gemm_t h, const void *X, const void *B1, void *H, gemm_rs_str
     a.epoch = ++h->epoch;
     a.timeout = h->timeout;
     a.skip_copies = (h->debug_flags & AG_GEMM_DEBUG_SKIP_COPIES) ? 1 : 0;
+    a.b4d = h->tmB_4d;
 
     const int64_t pairs = h->clusters;
     const int grid = static_cast<int>(2 * (a.total < pairs ? a.total : pairs));

@@ -62,6 +62,7 @@ struct AgArgs {
     uint32_t epoch;  // this call's index: a chunk is ready at epoch * nslices
     unsigned long long timeout;
     int skip_copies; // debug: deliver nothing, so remote-chunk waits run out
+    int b4d;         // 1: B1's map is 4D (one box per stage), 0: 3D (one per 64 columns)
 };
 
 constexpr uint32_t kBarCopy = 2; // named barrier of the 128 copy threads
@@ -69,18 +70,26 @@ constexpr uint32_t kBarCopy = 2; // named barrier of the 128 copy threads
 // Decode entry g of the AG order: rank r = g / T (T = nMs*nN tiles per rank);
 // inside a rank, chunk step s (chunk (r+s) mod W), then column tile nt, then
 // the chunk's 256-row tile.
-__host__ __device__ __forceinline__ void ag_decode(const AgArgs &g, int64_t e, int &r, int &mt2, int &nt,
-                                                   int &c)
+// 32-bit arithmetic: the host bounds the entry count below 2^31.
+__host__ __device__ __forceinline__ void ag_decode(const AgArgs &g, int64_t e64, int &r, int &mt2,
+                                                   int &nt, int &c)
 {
-    const int64_t T = static_cast<int64_t>(g.nMs) * g.nN;
-    r = static_cast<int>(e / T);
-    const int64_t p = e - static_cast<int64_t>(r) * T;
-    const int64_t per_chunk = static_cast<int64_t>(g.cntp) * g.nN;
-    const int s = static_cast<int>(p / per_chunk);
-    const int64_t q = p - static_cast<int64_t>(s) * per_chunk;
-    c = (r + s) % g.W;
-    nt = static_cast<int>(q / g.cntp);
-    mt2 = c * g.cntp + static_cast<int>(q - static_cast<int64_t>(nt) * g.cntp);
+    const uint32_t e = static_cast<uint32_t>(e64);
+    const uint32_t T = static_cast<uint32_t>(g.nMs) * static_cast<uint32_t>(g.nN);
+    const uint32_t rr = e / T;
+    const uint32_t p = e - rr * T;
+    const uint32_t cntp = static_cast<uint32_t>(g.cntp);
+    const uint32_t per_chunk = cntp * static_cast<uint32_t>(g.nN);
+    const uint32_t s = p / per_chunk;
+    const uint32_t q = p - s * per_chunk;
+    uint32_t cc = rr + s;
+    if (cc >= static_cast<uint32_t>(g.W))
+        cc -= static_cast<uint32_t>(g.W);
+    const uint32_t n = q / cntp;
+    r = static_cast<int>(rr);
+    c = static_cast<int>(cc);
+    nt = static_cast<int>(n);
+    mt2 = static_cast<int>(cc * cntp + (q - n * cntp));
 }
 
 // Bounded wait for a chunk signal: true once *p has reached `target` (compared
@@ -166,11 +175,16 @@ __device__ __forceinline__ void run_ag_producer(const AgArgs &g, const KernelArg
                 ptx::tma_load_3d_pair(sa, tmX, fb_leader, kb * kBK, row, 0, pol);
             else
                 ptx::tma_load_3d_pair(sa, tmG, fb_leader, kb * kBK, row, r, pol);
+            if (g.b4d) {
+                ptx::tma_load_4d_pair(sa + Cfg::kABytes, tmB, fb_leader, 0, kb * kBK,
+                                      (nt * BN + static_cast<int>(crank) * (BN / 2)) / 64, r, pol);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-                ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
-                                      nt * BN + static_cast<int>(crank) * (BN / 2) + j * 64, kb * kBK,
-                                      r, pol);
+                for (int j = 0; j < BN / 128; ++j)
+                    ptx::tma_load_3d_pair(sa + Cfg::kABytes + j * 8192, tmB, fb_leader,
+                                          nt * BN + static_cast<int>(crank) * (BN / 2) + j * 64,
+                                          kb * kBK, r, pol);
+            }
             ++issued;
             if (++stage == Cfg::kStages) {
                 stage = 0;

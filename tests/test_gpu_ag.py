@@ -28,6 +28,7 @@ SHAPES = [
     (4, 2048, 1000, 136),          # two 256-row tiles per chunk, ragged N
     (2, 512, 8, 8),                # N = 8 and K = 8: TMA boxes larger than the tensors
     (4, 1024, 16, 24),             # small N and K, four ranks
+    (2, 512, 320, 64),             # N % 64 == 0, not % 256: the 4D B box runs past N (zeros)
 ]
 
 

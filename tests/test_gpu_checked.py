@@ -35,7 +35,7 @@ from helpers import inputs, oracle_y, run_gpu
 assert "checked" in b.gemm_rs_version(), b.gemm_rs_version()
 cases = 0
 shapes = [(2, 256, 256, 256), (3, 300, 520, 200), (8, 64, 512, 192), (1, 200, 72, 64),
-          (16, 16 * 9, 136, 72), (4, 512, 768, 128)]
+          (16, 16 * 9, 136, 72), (4, 512, 768, 128), (4, 512, 320, 128)]
 for (W, M, N, Kpr) in shapes:
     A, B, C = inputs(W, M, N, Kpr, "int", c_dist="int")
     ref = oracle_y(A, B, C, 0.5, 1.0, "fp32")
@@ -112,7 +112,7 @@ def test_checked_build_finds_no_access_out_of_bounds():
     r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT, tests=HERE)], env=env,
                        capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
-    assert "checked cases 144" in r.stdout
+    assert "checked cases 168" in r.stdout
     assert "checked ag cases 12" in r.stdout
     assert "checked big ok" in r.stdout
     assert "checked noalloc cases 3" in r.stdout

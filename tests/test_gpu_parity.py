@@ -26,6 +26,7 @@ SHAPES = [
     (1, 200, 72, 64),      # W = 1 is a plain GEMM; N below one tile
     (16, 16 * 9, 136, 72), # W = 16, 9-row chunks, ragged K
     (4, 512, 768, 128),    # several row tiles per chunk
+    (4, 512, 320, 128),    # N % 64 == 0 but not % 256: the last tile's B box runs past N (zeros)
 ]
 
 
