@@ -375,12 +375,13 @@ GEMM_RS_API int gemm_rs_run_noalloc(int64_t M, int64_t N, int64_t K, int W, floa
 /*
  * GEMM_RS_NOALLOC_SCRATCH_BYTES as compiled into this library (the size of its
  * static scratch), for callers and bindings that do not read this header.
+ * (Part of the no-alloc entry point; the pages have no counterpart.)
  */
 GEMM_RS_API size_t gemm_rs_noalloc_scratch_bytes(void);
 
 /*
  * The outcome of the last gemm_rs_run_noalloc call in the current context, for
- * callers without a handle.  Waits for `stream` (the stream of that call),
+ * callers without a handle (the pages have no counterpart).  Waits for `stream` (the stream of that call),
  * reads the status word of the static scratch, and clears it.  Allocates
  * nothing (the word is copied into a host variable).  Returns GEMM_RS_OK,
  * GEMM_RS_ERR_TIMEOUT (a device wait ran out; Y is not valid),

@@ -55,3 +55,32 @@ def test_kernel_identity_ignores_comments_but_not_code():
     assert bench.code_only(src) != bench.code_only(edited_code)
     assert '"a // b"' in bench.code_only(src)          # a string literal is kept whole
     assert "comment" not in bench.code_only(src) and "another" not in bench.code_only(src)
+
+
+def test_sustained_run_blocks_and_averages(monkeypatch):
+    """The sustained region times blocks of about 0.2 s of calls until the
+    requested wall time has passed, and reports their mean per call."""
+    from tensor_gemm_reduce_tcgen05_gb300.inputs import WORKLOADS
+    w = WORKLOADS["ffn_w8_m4096"]
+    seen = []
+
+    def fake_b2b(fn, n, stream):
+        seen.append(n)
+        return 0.5  # ms per call
+
+    monkeypatch.setattr(bench, "time_loop_b2b", fake_b2b)
+    res = bench.sustained_run(lambda: None, w, None, 0.02, False, None)
+    assert seen[0] >= 1 and all(n == 400 for n in seen[1:])  # 0.2 s / 0.5 ms
+    assert res["calls"] == 400 * (len(seen) - 1)
+    assert abs(res["ms_per_call"] - 0.5) < 1e-12
+    assert abs(res["tflops"] - w.flops / 0.5e-3 / 1e12) < 1e-6
+
+
+def test_headline_profile_is_current():
+    """The committed ncu summary of the default workload was taken on the
+    current kernel source and the default plan, so the bench line reports its
+    DRAM traffic (a stale summary would make it null)."""
+    plan = {"bm": 256, "bn": 256, "stages": 7, "grid": 152, "colgroup": 32, "rowgroup": 4,
+            "rank_order": 1, "reduce_mode": 0}
+    t = bench.recorded_traffic("gemm_rs_pair_kernel", "ffn_w8_m8192_bias", plan)
+    assert t is not None and 5e9 < t < 2e10
