@@ -126,7 +126,12 @@ enum {
     /* The TMA producer issues no loads, so the MMA warp's wait on the first
      * stage runs out.  This exercises the timeout path on the GPU without a
      * fault.  Use only together with a short gemm_rs_set_timeout_cycles. */
-    GEMM_RS_DEBUG_STALL_PRODUCER = 1
+    GEMM_RS_DEBUG_STALL_PRODUCER = 1,
+    /* gemm_rs_run_streamed issues its copies but not the ready words that
+     * follow them, so the kernel's wait for the first rank's operands runs
+     * out (with a short gemm_rs_set_timeout_cycles): the timeout path of the
+     * streamed call, without a fault. */
+    GEMM_RS_DEBUG_SKIP_READY = 2
 };
 
 /*
@@ -183,6 +188,40 @@ GEMM_RS_API int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, 
  */
 GEMM_RS_API int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
                 gemm_rs_stream_t stream);
+
+/*
+ * gemm_rs_run with the inputs still in host memory: the host-to-device copies
+ * overlap the kernel.  The pages overlap a GEMM with the communication of its
+ * operands at tile granularity (the all-gather feeding the GEMM's tiles in the
+ * order they are sent, "flux精读" §3); here the transfer is the one from the
+ * host, and the unit is one rank's operands.
+ *   A_host, B_host, C_host  host, pinned (page-locked) copies of A, B and C in
+ *                           the layouts of gemm_rs_run; C_host may be NULL when
+ *                           beta == 0.
+ *   Y_host                  host, pinned, [M][N] in y_dtype: receives Y.
+ *   A, B, C, Y              device buffers as for gemm_rs_run; A, B and C are
+ *                           overwritten with the host copies.
+ *   stream                  the kernel and the copy of Y back run on it.
+ *   copy_stream             a second stream (not stream, not the legacy NULL
+ *                           stream) for the host-to-device copies.
+ * On copy_stream the call first waits for this handle's previous streamed
+ * kernel (so a streamed call never overwrites operands that the previous one
+ * still reads; other work that reads A, B or C must be ordered before this call
+ * by the caller), then copies C, and then rank by rank A_r and B_r, each
+ * followed by a 32-bit
+ * ready word in the workspace (a stream memory operation, after a memory
+ * fence).  The kernel's TMA producer waits, bounded, for rank r's word before
+ * it loads rank r's first tile, and the epilogue for C's word before it reads
+ * C, so with the ranks one after another rank r computes while rank r+1 is
+ * still being copied.  Asynchronous: Y_host is complete once `stream` has
+ * reached this point.  Errors as for gemm_rs_run, plus ERR_ARG for a NULL
+ * host pointer or copy_stream == stream; a wait that runs out is reported by
+ * gemm_rs_status like any other timeout.
+ */
+GEMM_RS_API int gemm_rs_run_streamed(gemm_rs_t h, const void *A_host, const void *B_host,
+                                     const void *C_host, void *Y_host, void *A, void *B, void *C,
+                                     void *Y, gemm_rs_stream_t stream,
+                                     gemm_rs_stream_t copy_stream);
 
 /* Free the handle's host state.  Does not touch device memory.  NULL is a no-op. */
 GEMM_RS_API int gemm_rs_destroy(gemm_rs_t h);

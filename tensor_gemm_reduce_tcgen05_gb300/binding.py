@@ -37,6 +37,7 @@ GEMM_RS_ERR_WORKSPACE = -7
 GEMM_RS_ERR_BOUNDS = -8
 
 GEMM_RS_DEBUG_STALL_PRODUCER = 1
+GEMM_RS_DEBUG_SKIP_READY = 2
 
 GEMM_RS_REDUCE_CHAIN = 0
 GEMM_RS_REDUCE_LAST_ARRIVER = 1
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
             "gemm_rs_create": (i32, [ctypes.POINTER(vp), i64, i64, i64, i32, f32, f32, i32, i32,
                                      i32, vp, sz, vp]),
             "gemm_rs_run": (i32, [vp, vp, vp, vp, vp, vp]),
+            "gemm_rs_run_streamed": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "gemm_rs_destroy": (i32, [vp]),
             "gemm_rs_last_error": (ctypes.c_char_p, []),
             "gemm_rs_status": (i32, [vp, vp]),
@@ -149,6 +151,11 @@ def gemm_rs_create(M, N, K, W, alpha, beta, ab_dtype, c_dtype, y_dtype, workspac
 
 def gemm_rs_run(h, A, B, C, Y, stream=0) -> None:
     _check(lib().gemm_rs_run(h, A, B, C, Y, stream))
+
+
+def gemm_rs_run_streamed(h, A_host, B_host, C_host, Y_host, A, B, C, Y, stream, copy_stream) -> None:
+    _check(lib().gemm_rs_run_streamed(h, A_host, B_host, C_host, Y_host, A, B, C, Y, stream,
+                                      copy_stream))
 
 
 def gemm_rs_destroy(h) -> None:
@@ -305,6 +312,28 @@ class GemmRS:
             Y = self.new_output()
         gemm_rs_run(self.handle, A.data_ptr(), B.data_ptr(), 0 if C is None else C.data_ptr(),
                     Y.data_ptr(), _stream_ptr(stream))
+        return Y
+
+    def run_streamed(self, A_host, B_host, C_host, Y_host, A, B, C=None, Y=None, stream=None,
+                     copy_stream=None):
+        """gemm_rs_run_streamed: copy pinned host inputs into A, B (and C) on
+        copy_stream, rank by rank, while the kernel on `stream` consumes the
+        ranks that have landed; Y goes back into Y_host on `stream`.  Returns
+        Y (device)."""
+        import torch
+        for t, name in ((A_host, "A_host"), (B_host, "B_host"), (Y_host, "Y_host")):
+            if t.device.type != "cpu" or not t.is_pinned() or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous pinned host tensor")
+        if C_host is not None and (not C_host.is_pinned() or not C_host.is_contiguous()):
+            raise ValueError("C_host must be a contiguous pinned host tensor")
+        if Y is None:
+            Y = self.new_output()
+        if copy_stream is None:
+            raise ValueError("copy_stream is required (a stream other than `stream`)")
+        gemm_rs_run_streamed(self.handle, A_host.data_ptr(), B_host.data_ptr(),
+                             0 if C_host is None else C_host.data_ptr(), Y_host.data_ptr(),
+                             A.data_ptr(), B.data_ptr(), 0 if C is None else C.data_ptr(),
+                             Y.data_ptr(), _stream_ptr(stream), _stream_ptr(copy_stream))
         return Y
 
     def status(self, stream=None) -> int:

@@ -292,6 +292,11 @@ struct gemm_rs_s {
     unsigned long long timeout;
     int32_t *record;
     int debug_flags;
+    // gemm_rs_run_streamed: the call index its ready words carry, and an event
+    // after its latest kernel (the next call's copies wait for it)
+    uint32_t stream_epoch;
+    cudaEvent_t streamed_done;
+    bool streamed_pending;
 };
 
 namespace {
@@ -421,12 +426,17 @@ int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, int W, float
     h->timeout = 1ull << 32;
     h->record = nullptr;
     h->debug_flags = 0;
+    h->stream_epoch = 0;
+    h->streamed_done = nullptr;
+    h->streamed_pending = false;
     *out = h;
     return GEMM_RS_OK;
 }
 
 int gemm_rs_destroy(gemm_rs_t h)
 {
+    if (h != nullptr && h->streamed_done != nullptr)
+        cudaEventDestroy(h->streamed_done);
     delete h;
     return GEMM_RS_OK;
 }
@@ -543,7 +553,7 @@ int gemm_rs_set_debug(gemm_rs_t h, int32_t *record, int flags)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
-    if (flags & ~GEMM_RS_DEBUG_STALL_PRODUCER)
+    if (flags & ~(GEMM_RS_DEBUG_STALL_PRODUCER | GEMM_RS_DEBUG_SKIP_READY))
         return fail(GEMM_RS_ERR_ARG, "unknown debug flags 0x%x", flags);
     if (record != nullptr && !aligned(record, 16))
         return fail(GEMM_RS_ERR_ALIGN, "record buffer must be 16-byte aligned");
@@ -552,8 +562,15 @@ int gemm_rs_set_debug(gemm_rs_t h, int32_t *record, int flags)
     return GEMM_RS_OK;
 }
 
-int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
-                gemm_rs_stream_t stream)
+} // extern "C"
+
+namespace {
+
+// One launch of the fused kernel for gemm_rs_run and gemm_rs_run_streamed.
+// ready: NULL, or the ready words the kernel waits on before it reads the
+// inputs (rank r's A_r and B_r, then C), which reach `epoch` when they land.
+int run_impl(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
+             gemm_rs_stream_t stream, const uint32_t *ready, uint32_t epoch)
 {
     if (h == nullptr)
         return fail(GEMM_RS_ERR_ARG, "handle is NULL");
@@ -634,6 +651,8 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     a.timeout = h->timeout;
     a.stall_producer = (h->debug_flags & GEMM_RS_DEBUG_STALL_PRODUCER) ? 1 : 0;
     a.b4d = h->Kpr > 0 ? h->tmB_4d : 0;
+    a.ready = ready;
+    a.epoch = epoch;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (h->bm == 2 * gemm_rs::kBM) {
@@ -662,6 +681,116 @@ int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused GEMM+RS kernel");
+    return GEMM_RS_OK;
+}
+
+// Ready words of the streamed call: 32-bit words inside the workspace's
+// 256-byte status block, from byte 128 (W <= 16 ranks and C: at most 68 bytes).
+constexpr size_t kReadyOff = 128;
+
+using WriteValue32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+// cuStreamWriteValue32 from the driver, looked up once.
+int get_write_value(WriteValue32 *out)
+{
+    static WriteValue32 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+            return fail(GEMM_RS_ERR_CUDA, "cuStreamWriteValue32 is not available from the driver");
+        fn = reinterpret_cast<WriteValue32>(p);
+    }
+    *out = fn;
+    return GEMM_RS_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
+                gemm_rs_stream_t stream)
+{
+    return run_impl(h, A, B, C, Y, stream, nullptr, 0);
+}
+
+int gemm_rs_run_streamed(gemm_rs_t h, const void *A_host, const void *B_host, const void *C_host,
+                         void *Y_host, void *A, void *B, void *C, void *Y, gemm_rs_stream_t stream,
+                         gemm_rs_stream_t copy_stream)
+{
+    if (h == nullptr)
+        return fail(GEMM_RS_ERR_ARG, "handle is NULL");
+    if (copy_stream == nullptr || copy_stream == stream)
+        return fail(GEMM_RS_ERR_ARG, "copy_stream must be a stream of its own, not stream or NULL");
+    if (Y_host == nullptr || (h->Kpr > 0 && (A_host == nullptr || B_host == nullptr)) ||
+        (h->beta != 0.0f && C_host == nullptr))
+        return fail(GEMM_RS_ERR_ARG, "a host buffer is NULL");
+    if (h->M == 0 || h->N == 0)
+        return GEMM_RS_OK;
+    if (Y == nullptr || (h->Kpr > 0 && (A == nullptr || B == nullptr)) ||
+        (h->beta != 0.0f && C == nullptr))
+        return fail(GEMM_RS_ERR_ARG, "a device buffer is NULL");
+    WriteValue32 write_value;
+    int rc = get_write_value(&write_value);
+    if (rc != GEMM_RS_OK)
+        return rc;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(copy_stream);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (h->streamed_done == nullptr &&
+        (e = cudaEventCreateWithFlags(&h->streamed_done, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreateWithFlags");
+    // the previous streamed kernel of this handle no longer reads A, B and C
+    if (h->streamed_pending && (e = cudaStreamWaitEvent(cs, h->streamed_done, 0)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamWaitEvent(copy stream)");
+    if (++h->stream_epoch == 0)
+        h->stream_epoch = 1;
+    const uint32_t epoch = h->stream_epoch;
+    uint32_t *ready = reinterpret_cast<uint32_t *>(h->ws + kReadyOff);
+    const bool skip = (h->debug_flags & GEMM_RS_DEBUG_SKIP_READY) != 0;
+    auto mark = [&](int i) -> int {
+        if (skip)
+            return GEMM_RS_OK;
+        const CUresult r = write_value(reinterpret_cast<CUstream>(cs),
+                                       reinterpret_cast<CUdeviceptr>(ready + i), epoch, 0);
+        return r == CUDA_SUCCESS ? GEMM_RS_OK
+                                 : fail(GEMM_RS_ERR_CUDA, "cuStreamWriteValue32 failed (CUresult %d)",
+                                        (int)r);
+    };
+    // C first (every rank's epilogue reads it), then rank by rank
+    if (h->beta != 0.0f) {
+        if ((e = cudaMemcpyAsync(C, C_host, static_cast<size_t>(h->M * h->N) * 2,
+                                 cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(C)");
+        if ((rc = mark(h->W)) != GEMM_RS_OK)
+            return rc;
+    }
+    const size_t a_rank = static_cast<size_t>(h->M * h->Kpr) * 2;
+    const size_t b_rank = static_cast<size_t>(h->Kpr * h->N) * 2;
+    for (int r = 0; r < h->W; ++r) {
+        if (h->Kpr > 0) {
+            if ((e = cudaMemcpyAsync(static_cast<uint8_t *>(A) + r * a_rank,
+                                     static_cast<const uint8_t *>(A_host) + r * a_rank, a_rank,
+                                     cudaMemcpyHostToDevice, cs)) != cudaSuccess ||
+                (e = cudaMemcpyAsync(static_cast<uint8_t *>(B) + r * b_rank,
+                                     static_cast<const uint8_t *>(B_host) + r * b_rank, b_rank,
+                                     cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+                return cuda_fail(e, "cudaMemcpyAsync(A_r, B_r)");
+        }
+        if ((rc = mark(r)) != GEMM_RS_OK)
+            return rc;
+    }
+    if ((rc = run_impl(h, A, B, h->beta != 0.0f ? C : nullptr, Y, stream, ready, epoch)) != GEMM_RS_OK)
+        return rc;
+    if ((e = cudaEventRecord(h->streamed_done, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord");
+    h->streamed_pending = true;
+    const size_t y_bytes = static_cast<size_t>(h->M * h->N) * (h->y_dtype == GEMM_RS_FP32 ? 4 : 2);
+    if ((e = cudaMemcpyAsync(Y_host, Y, y_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(Y)");
     return GEMM_RS_OK;
 }
 

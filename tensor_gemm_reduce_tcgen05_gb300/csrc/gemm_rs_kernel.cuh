@@ -144,6 +144,10 @@ struct KernelArgs {
     unsigned long long timeout;
     int stall_producer;
     int b4d;        // 1: the B tensor map is 4D (one load per stage), 0: 3D (one per 64 columns)
+    // Host-streamed inputs (gemm_rs_run_streamed): ready[r] reaches `epoch` once
+    // rank r's A_r and B_r have landed, ready[W] once C has; NULL otherwise.
+    const uint32_t *ready;
+    uint32_t epoch;
 };
 
 struct SmemCtl {
@@ -230,6 +234,37 @@ __device__ __forceinline__ void report(const KernelArgs &a, SmemCtl *ctl, uint32
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// Host-streamed inputs: wait until the ready word *p has reached `epoch`
+// (compared modulo 2^32), with acquire semantics, so that the copy it follows
+// is visible.  Bounded by `limit` SM cycles; false when it runs out or the CTA
+// aborts.
+__device__ __forceinline__ bool wait_ready(const uint32_t *p, uint32_t epoch,
+                                           unsigned long long limit, const volatile int *abort)
+{
+    const long long t0 = clock64();
+    while (static_cast<int32_t>(ptx::ld_acquire_gpu(p) - epoch) < 0) {
+        if (*abort != 0 || static_cast<unsigned long long>(clock64() - t0) > limit)
+            return false;
+        __nanosleep(256);
+    }
+    return true;
+}
+
+// Before a producer loads rank r's operands: with host-streamed inputs, wait
+// for rank r's copy once (a bit per rank remembers it), then order the copy's
+// writes before the TMA reads (async proxy).
+__device__ __forceinline__ bool operands_ready(const KernelArgs &a, int r, uint32_t &seen,
+                                               const volatile int *abort)
+{
+    if (a.ready == nullptr || ((seen >> r) & 1u))
+        return true;
+    if (!wait_ready(a.ready + r, a.epoch, a.timeout, abort))
+        return false;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    seen |= 1u << r;
+    return true;
+}
+
 // Epilogue threads: warps 2-5, or warps 2-9 in the chain mode (which has no
 // reduce jobs for warps 6-9 to take).
 __device__ __forceinline__ int epi_threads(const KernelArgs &a) { return a.chain ? 256 : 128; }
@@ -246,6 +281,7 @@ __device__ __forceinline__ void run_producer(const KernelArgs &a, const Sched &s
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
+    uint32_t ranks_ready = 0;
     if (!a.stall_producer) {
         for (int64_t g = blockIdx.x; g < a.total && ok; g += gridDim.x) {
             int r, mt, nt;
@@ -256,6 +292,10 @@ __device__ __forceinline__ void run_producer(const KernelArgs &a, const Sched &s
                 rec[1] = mt;
                 rec[2] = nt;
                 rec[3] = static_cast<int32_t>(blockIdx.x);
+            }
+            if (!operands_ready(a, r, ranks_ready, abort_flag)) {
+                ok = false;
+                break;
             }
             for (int kb = 0; kb < a.nK; ++kb) {
                 if (!ptx::mbar_wait(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,
@@ -701,6 +741,14 @@ __device__ __forceinline__ void run_epilogue(const KernelArgs &a, const Sched &s
     bool ok = true;
     uint32_t rq_n = 0;
     int it = 0;
+    // Host-streamed inputs: C must have landed before the first read of it.
+    // Thread 0 waits; the first tile's barrier passes a failure on and orders
+    // the other threads' reads after its acquire.
+    if (a.ready != nullptr && a.C != nullptr && etid == 0 &&
+        !wait_ready(a.ready + a.W, a.epoch, a.timeout, abort_flag)) {
+        report(a, ctl, kStatusTimeoutEpilogue);
+        ok = false;
+    }
     for (int64_t g = g0; g < a.total; g += gstride, ++it) {
         int r, mts, nt, pos;
         decode_tile(sch, g, r, mts, nt, pos);
@@ -1148,6 +1196,7 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
+    uint32_t ranks_ready = 0;
     if (!a.stall_producer) {
         for (int64_t g = cid; g < a.total && ok; g += ncl) {
             int r, mt2, nt;
@@ -1158,6 +1207,10 @@ __device__ __forceinline__ void run_producer_pair(const KernelArgs &a, const Sch
                 rec[1] = mt2;
                 rec[2] = nt;
                 rec[3] = static_cast<int32_t>(cid);
+            }
+            if (!operands_ready(a, r, ranks_ready, abort_flag)) {
+                ok = false;
+                break;
             }
             for (int kb = 0; kb < a.nK; ++kb) {
                 if (!ptx::mbar_wait_cluster(ptx::smem_u32(&ctl->empty[stage]), phase ^ 1u, a.timeout,

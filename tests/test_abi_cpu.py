@@ -227,6 +227,8 @@ def test_null_handle_calls_fail_cleanly(b):
     for fn in (b.lib().gemm_rs_status, b.lib().gemm_rs_reset):
         assert fn(None, None) == b.GEMM_RS_ERR_ARG
     assert b.lib().gemm_rs_run(None, None, None, None, None, None) == b.GEMM_RS_ERR_ARG
+    assert b.lib().gemm_rs_run_streamed(None, None, None, None, None, None, None, None, None,
+                                        None, None) == b.GEMM_RS_ERR_ARG
     assert b.lib().gemm_rs_destroy(None) == 0
     with pytest.raises(b.GemmRSError):
         b.gemm_rs_schedule(255, 256, 2, 128, 256)
