@@ -103,3 +103,29 @@ def test_streamed_wait_times_out_and_recovers(tile):
     b.gemm_rs_set_timeout_cycles(op.handle, 1 << 32)
     y = _streamed(op, A, B, C, "fp32", Ad, Bd, Cd, stream, copy_stream)
     np.testing.assert_array_equal(y, oracle_y(A, B, C, 1.0, 0.5, "fp32"))
+
+
+def test_streamed_rejects_bad_streams_and_buffers():
+    """The copy stream must be a stream of its own, and every host buffer the
+    call needs must be given; the checks fail before anything is enqueued."""
+    from tensor_gemm_reduce_tcgen05_gb300 import binding as b
+    W, M, N, Kpr = 2, 256, 256, 64
+    dev = torch.device("cuda", 0)
+    op = b.GemmRS(M, N, W * Kpr, W, 1.0, 0.5, "fp32", device=dev)
+    A = torch.zeros((W, M, Kpr), dtype=torch.bfloat16, pin_memory=True)
+    B = torch.zeros((W, Kpr, N), dtype=torch.bfloat16, pin_memory=True)
+    C = torch.zeros((M, N), dtype=torch.bfloat16, pin_memory=True)
+    Yh = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    Ad, Bd, Cd, Y = A.to(dev), B.to(dev), C.to(dev), op.new_output()
+    s = torch.cuda.Stream(device=dev)
+    L = b.lib()
+    args = [A.data_ptr(), B.data_ptr(), C.data_ptr(), Yh.data_ptr(), Ad.data_ptr(), Bd.data_ptr(),
+            Cd.data_ptr(), Y.data_ptr()]
+    assert L.gemm_rs_run_streamed(op.handle, *args, s.cuda_stream, s.cuda_stream) == b.GEMM_RS_ERR_ARG
+    assert L.gemm_rs_run_streamed(op.handle, *args, s.cuda_stream, None) == b.GEMM_RS_ERR_ARG
+    no_c = list(args)
+    no_c[2] = None  # beta != 0 needs C_host
+    other = torch.cuda.Stream(device=dev)
+    assert L.gemm_rs_run_streamed(op.handle, *no_c, s.cuda_stream, other.cuda_stream) == \
+        b.GEMM_RS_ERR_ARG
+    assert "host buffer" in b.gemm_rs_last_error()
