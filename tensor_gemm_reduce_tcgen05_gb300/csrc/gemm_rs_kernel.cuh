@@ -572,17 +572,21 @@ __device__ __forceinline__ uint32_t chain_k(uint32_t s) { return (s >> 16) & 31u
 // owns the tile, and the caller now owns it; `seen` is then the state it took
 // the tile in (its pending bits tell which positions after i are stored).  The
 // first compare-and-swap guesses `guess` (by default the usual state: k = i,
-// nothing stored ahead), so the common case costs one atomic.
+// nothing stored ahead), so the common case costs one atomic.  Taking the fold
+// publishes nothing, so the compare-and-swap only acquires: the additions and
+// slots of positions 0 .. k-1 (released by whoever published k) are ordered
+// before the caller's.  A release here would add a gpu-scope fence per tile,
+// which on this two-die part is broadcast to the other die's L2 slices.
 __device__ __forceinline__ bool chain_try_own(uint32_t *flag, uint32_t i, uint32_t guess,
                                               uint32_t &seen)
 {
-    uint32_t s = ptx::atom_cas_acq_rel_gpu(flag, guess, guess | kChainOwn);
+    uint32_t s = ptx::atom_cas_acquire_gpu(flag, guess, guess | kChainOwn);
     if (s == guess) {
         seen = s;
         return true;
     }
     while (chain_k(s) == i && !(s & kChainOwn)) {
-        const uint32_t prev = ptx::atom_cas_acq_rel_gpu(flag, s, s | kChainOwn);
+        const uint32_t prev = ptx::atom_cas_acquire_gpu(flag, s, s | kChainOwn);
         if (prev == s) {
             seen = s;
             return true;

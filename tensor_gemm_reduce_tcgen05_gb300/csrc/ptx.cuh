@@ -427,6 +427,19 @@ __device__ __forceinline__ uint32_t atom_cas_acq_rel_gpu(uint32_t *p, uint32_t e
     return old;
 }
 
+// Compare-and-swap with acquire semantics only: orders the caller's later
+// accesses after the writes that the value found was released with, and
+// publishes nothing of the caller's (no release fence before it).
+__device__ __forceinline__ uint32_t atom_cas_acquire_gpu(uint32_t *p, uint32_t expect, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acquire.gpu.global.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(old)
+                 : "l"(p), "r"(expect), "r"(v)
+                 : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
 {
     uint32_t v;
