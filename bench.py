@@ -410,8 +410,8 @@ def chunked_baseline(W, M, N, alpha, beta, y_code, Ad, Bd, Cd, Y, stream, dev):
 def time_loop(fn, steps, stream):
     """Mean ms per call over `steps` calls of fn on `stream`.  Each call is
     bracketed by its own event pair, the pattern of the fused arm's timed
-    region (whose per-call events give the kernel durations), so every arm
-    pays the same event overhead between calls."""
+    region when an L2 flush separates its calls, so every arm pays the same
+    event overhead between calls."""
     import torch
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
@@ -560,7 +560,13 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
 
-    # ---- timed region: K fused calls, events around each launch
+    # ---- timed region: K fused calls.  With an L2 flush between calls, events
+    # around each launch give the calls' own device time.  Without one, the K
+    # calls run back to back between two events: an event recorded between two
+    # launches would keep a call's prologue (barrier and TMEM set-up, before its
+    # griddepcontrol.wait) from overlapping the previous call, which a caller
+    # issuing calls back to back gets.  The average launch duration is then the
+    # region over K (the region holds nothing but the K launches).
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
@@ -572,21 +578,35 @@ def run_ours(args):
     for i in range(args.steps):
         if cold:
             flush_l2()
-        starts[i].record(stream)
+            starts[i].record(stream)
         step()
-        ends[i].record(stream)
+        if cold:
+            ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kernel_avg_ms = sum(kernel_ms) / len(kernel_ms)
-    # with a flush between calls the step time is the calls' own device time
-    ms_step = kernel_avg_ms if cold else t0.elapsed_time(t1) / args.steps
+    if op.status(stream) != 0:
+        raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+    if cold:
+        kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        kernel_avg_ms = sum(kernel_ms) / len(kernel_ms)
+        ms_step = kernel_avg_ms
+    else:
+        ms_step = t0.elapsed_time(t1) / args.steps
+        kernel_avg_ms = ms_step
+        # the spread of single calls, each between its own events (diagnostic)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kernel_sorted = sorted(kernel_ms)
     kernel_median_ms = kernel_sorted[len(kernel_sorted) // 2]
     kernel_min_ms = kernel_sorted[0]
-    if op.status(stream) != 0:
-        raise RuntimeError("device timeout in the timed region: " + binding.gemm_rs_last_error())
+    kernel_note = ("each timed call between its own events, an L2 flush before each" if cold else
+                   "kernel_ms: the back-to-back timed region over its launches; median and min: "
+                   "calls timed one at a time between their own events after the region")
 
     ms_step_max = max_over_ranks(dist, ms_step, dev)
     value = aggregate_throughput(w.flops, world, ms_step_max / 1e3) / 1e12
@@ -613,7 +633,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
                 "kernel_ms": kernel_avg_ms, "kernel_ms_median": kernel_median_ms,
-                "kernel_ms_min": kernel_min_ms, "config": workload_config(w), "plan": op.plan,
+                "kernel_ms_min": kernel_min_ms, "kernel_ms_note": kernel_note,
+                "config": workload_config(w), "plan": op.plan,
                 "clocks": clocks, "sustained": sustained, "clocks_rest": rest,
                 "note": "profiling run: fused kernel only"}
         if rank == 0:
@@ -685,16 +706,24 @@ def run_ours(args):
 
     for _ in range(max(3, args.warmup)):
         unfused()
-    # fused and unfused in interleaved rounds (the same clocks for both)
+    # fused and unfused in interleaved rounds (the same clocks for both), each
+    # call timed the way the fused arm's timed region times it: back to back,
+    # or between its own events where an L2 flush separates the calls; the
+    # other way is reported beside it
     rounds, per_round = 4, max(3, args.steps // 4)
-    pair = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream)
+    main_timer, other_timer = (time_loop, time_loop_b2b) if cold else (time_loop_b2b, time_loop)
+    pair = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream,
+                       timer=main_timer)
     unfused_ms = pair["unfused"]
     gemms_ms = time_loop(gemms, args.steps, stream)
     reduce_ms = time_loop(reduce_only, args.steps, stream)
-    b2b = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream,
-                      timer=time_loop_b2b)
-    b2b = {"fused_ms": b2b["fused"], "unfused_ms": b2b["unfused"],
-           "fused_speedup": b2b["unfused"] / b2b["fused"]}
+    other = interleaved({"fused": step, "unfused": unfused}, rounds, per_round, stream,
+                        timer=other_timer)
+    other = {"fused_ms": other["fused"], "unfused_ms": other["unfused"],
+             "fused_speedup": other["unfused"] / other["fused"],
+             "note": ("calls issued in a row with no events between them" if cold else
+                      "each call between its own events, which keeps a call's prologue from "
+                      "overlapping the previous call")}
     del P
 
     # chunked two-stream baseline (async-TP style)
@@ -703,7 +732,8 @@ def run_ours(args):
     if p_dtype == binding.GEMM_RS_FP32:
         for _ in range(max(3, args.warmup)):
             chunked()
-        cp = interleaved({"fused": step, "chunked": chunked}, rounds, per_round, stream)
+        cp = interleaved({"fused": step, "chunked": chunked}, rounds, per_round, stream,
+                         timer=main_timer)
         chunked_ms, chunked_fused_ms = cp["chunked"], cp["fused"]
     del chunked
 
@@ -760,7 +790,7 @@ def run_ours(args):
     for fn in arms.values():
         for _ in range(3):
             fn()
-    res = interleaved(arms, rounds, per_round, stream)
+    res = interleaved(arms, rounds, per_round, stream, timer=main_timer)
     other_mode = {}
     for name, m in modes.items():
         if m == mode0:
@@ -834,7 +864,9 @@ def run_ours(args):
                         "fused_ms_interleaved": pair["fused"],
                         "fused_speedup": unfused_ms / pair["fused"],
                         "note": f"fused and unfused timed in {rounds} interleaved rounds of "
-                                f"{per_round} calls each, order reversed every round"},
+                                f"{per_round} calls each, order reversed every round, "
+                                + ("each call between its own events" if cold else
+                                   "the calls of a round back to back")},
             "unfused_chunked": None if chunked_ms is None else {
                 "ms_per_step": chunked_ms, "value": w.flops / (chunked_ms / 1e3) / 1e12,
                 "chunks": w.W, "fused_speedup": chunked_ms / chunked_fused_ms,
@@ -843,13 +875,13 @@ def run_ours(args):
             "full_k_gemm": {"ms": fullk_ms, "value": w.flops / (fullk_ms / 1e3) / 1e12,
                             "note": "torch.mm [M,K]x[K,N], no reduce-scatter (context)"},
             "kernel_ms_median": kernel_median_ms, "kernel_ms_min": kernel_min_ms,
+            "kernel_ms_note": kernel_note,
             "cold_l2": {"kernel_ms_median": cold_ms[len(cold_ms) // 2], "kernel_ms_min": cold_ms[0],
                         "calls": n_cold, "flush_bytes": FLUSH_BYTES},
             "ablation": {"kernel_batched_ms": ms_step, "kernel_sync_ms": ks_ms,
                          "clear_kernel_sync_ms": cks_ms},
             "other_reduce_mode": other_mode,
-            "back_to_back": dict(b2b, note="calls issued in a row with no events between "
-                                 "them; every other figure brackets each call with events"),
+            "other_timing": other,
             "plan": plan,
         }
         print(json.dumps(line))
