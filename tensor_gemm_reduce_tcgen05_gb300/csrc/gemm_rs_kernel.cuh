@@ -12,9 +12,11 @@
 //
 // Warp roles (320 threads):
 //   warp 0      TMA producer (one thread).  For each k-block it loads the A_r
-//               box [128 x 64] and the B_r boxes [64 x 64] into a stage of the
-//               shared-memory ring, 128-byte swizzled, completing the stage's
-//               `full` mbarrier.
+//               box [128 x 64] and the B_r tile [64 x BN] (one 4D box of BN/64
+//               64-column atoms, or one 3D box per atom when N is not a
+//               multiple of 64) into a stage of the shared-memory ring,
+//               128-byte swizzled, completing the stage's `full` mbarrier.  In
+//               a host-streamed call it first waits for rank r's ready word.
 //   warp 1      TMEM allocator and MMA issuer (one thread).  It issues
 //               tcgen05.mma (bf16 -> fp32) into one of two TMEM accumulators;
 //               tcgen05.commit frees each stage and, at the end of the tile,
@@ -46,7 +48,8 @@
 // "flux实现：sm80 gemm+rs", section "device side barrier").  CHAIN has one,
 // bounded: a position may wait a few thousand cycles for the position before
 // it, which lies earlier in the tile order, so the waits form no cycle.
-// Every mbarrier wait is bounded in SM cycles too.  A wait that runs out
+// Every mbarrier wait, and every wait for a streamed call's ready word, is
+// bounded in SM cycles too.  A wait that runs out
 // records a code in the status word, and the CTA drains its TMA loads and
 // MMAs, frees TMEM and exits.
 //
