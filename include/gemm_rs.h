@@ -185,6 +185,13 @@ GEMM_RS_API int gemm_rs_create(gemm_rs_t *out, int64_t M, int64_t N, int64_t K, 
  * the host when the pointers change.  Returns ERR_ARG / ERR_ALIGN for bad
  * pointers and ERR_CUDA if the launch fails.  A device-side timeout is not
  * seen here: call gemm_rs_status.
+ * The launch uses programmatic stream serialization: the kernel may start its
+ * shared-memory and TMEM set-up while the previous kernel on `stream` is
+ * still finishing, and waits for that kernel to complete (griddepcontrol.wait)
+ * before its first global memory access, so every read and write is ordered
+ * after the earlier work on the stream as for any launch.  Calls issued back
+ * to back overlap by that set-up; an event recorded between them removes the
+ * overlap.
  */
 GEMM_RS_API int gemm_rs_run(gemm_rs_t h, const void *A, const void *B, const void *C, void *Y,
                 gemm_rs_stream_t stream);
