@@ -228,26 +228,19 @@ int pick_rowgroup(int64_t M, int64_t Kpr, int W, int bm, int live)
 // contributions to one output tile lie at least 1.25 waves of workers apart,
 // so that they arrive in step order.
 //
-// Ranks one after another (live = 1): one rank's operands stay in L2 through
-// its pass whatever the group, but the running sums of a group (M x its
-// columns, fp32) stay live across all W passes.  Two groups are used when
-// that halves them to at most 40 MB, so that they stay in L2 for the price of
-// reading A twice, and when a rank's pass over half the columns still keeps a
-// tile's consecutive contributions 1.25 waves apart; otherwise one group.
+// Ranks one after another (live = 1): one group.  One rank's operands stay in
+// L2 through its pass whatever the group.  Two groups would keep half the
+// running sums (M x half the columns, fp32) live across the W passes, for the
+// price of reading A twice, but timed in interleaved rounds they were no
+// faster at W=8 M=N=4096 (32 MB of sums per group) and 11-14 % slower with
+// the MMA loop that issues one multicast commit per stage.
 int pick_colgroup(int64_t M, int64_t N, int64_t Kpr, int W, int bm, int bn, int64_t workers,
                   int live)
 {
     const int64_t nN = cdiv(N, bn);
     const int64_t nMs = cdiv(M, bm);
-    if (live == 1) {
-        const int64_t half = cdiv(nN, 2);
-        const double rs_half = 4.0 * static_cast<double>(M) * half * bn;
-        // consecutive ranks' contributions to a tile: about nMs*G*(W-2)/W items apart
-        const double sep = static_cast<double>(nMs) * half * (W - 2) / W;
-        const bool split = nN > 1 && rs_half <= 40.0 * (1 << 20) &&
-                           sep >= 1.25 * static_cast<double>(workers);
-        return static_cast<int>(split ? half : nN);
-    }
+    if (live == 1)
+        return static_cast<int>(nN);
     const double a_bytes = 2.0 * W * M * Kpr;
     const double b_bytes = 2.0 * W * Kpr * N;
     const double budget = 64.0 * (1 << 20);

@@ -366,6 +366,17 @@ __device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     int it = 0;
+    // The MMA thread's loop is on the critical path (the tensor pipe idles
+    // while it prepares the next k-block), so the descriptors of stage 0 are
+    // built once and moved to a stage and K step by additions.
+    // A: K-major, rows of 128 bytes, 8-row groups 1024 bytes apart; K step of
+    //    16 elements = 32 bytes inside the swizzle atom.
+    // B: MN-major, 64-column atoms 8192 bytes apart (LBO), 8-row K groups 1024
+    //    bytes apart (SBO); K step of 16 rows = 2048 bytes.
+    const uint32_t s0 = ptx::smem_u32(smem);
+    const uint64_t ad0 = ptx::sdesc_sw128(s0, 0, 1024);
+    const uint64_t bd0 = ptx::sdesc_sw128(s0 + Cfg::kABytes, 8192, 1024);
+    const uint32_t empty0 = ptx::smem_u32(&ctl->empty[0]);
     for (int64_t g = blockIdx.x; g < a.total; g += gridDim.x, ++it) {
         const int buf = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
@@ -381,19 +392,13 @@ __device__ __forceinline__ void run_mma(const KernelArgs &a, uint32_t tmem, uint
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
-            const uint32_t sb = sa + Cfg::kABytes;
+            const uint32_t so = stage * Cfg::kStageBytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                // A: K-major, rows of 128 bytes, 8-row groups 1024 bytes apart;
-                //    K step of 16 elements = 32 bytes inside the swizzle atom.
-                // B: MN-major, 64-column atoms 8192 bytes apart (LBO), 8-row K
-                //    groups 1024 bytes apart (SBO); K step of 16 rows = 2048 bytes.
-                const uint64_t ad = ptx::sdesc_sw128(sa + kk * 32, 0, 1024);
-                const uint64_t bd = ptx::sdesc_sw128(sb + kk * 2048, 8192, 1024);
-                ptx::mma_bf16_ss(d, ad, bd, Cfg::kIdesc, (kb | kk) != 0 ? 1u : 0u);
-            }
-            ptx::mma_commit(ptx::smem_u32(&ctl->empty[stage]));
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                ptx::mma_bf16_ss(d, ptx::sdesc_advance(ad0, so + kk * 32),
+                                 ptx::sdesc_advance(bd0, so + kk * 2048), Cfg::kIdesc,
+                                 (kb | kk) != 0 ? 1u : 0u);
+            ptx::mma_commit(empty0 + stage * 8u);
             if (++stage == Cfg::kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -1283,6 +1288,14 @@ __device__ __forceinline__ void run_mma_pair(const KernelArgs &a, uint32_t tmem,
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     int it = 0;
+    // As in run_mma: stage 0's descriptors, moved by additions.  They describe
+    // this CTA's 128 rows of A and BN/2 columns of B; the peer CTA holds its
+    // halves at the same offsets.  One multicast commit releases a stage in
+    // both CTAs.
+    const uint32_t s0 = ptx::smem_u32(smem);
+    const uint64_t ad0 = ptx::sdesc_sw128(s0, 0, 1024);
+    const uint64_t bd0 = ptx::sdesc_sw128(s0 + Cfg::kABytes, 8192, 1024);
+    const uint32_t empty0 = ptx::smem_u32(&ctl->empty[0]);
     for (int64_t g = cid; g < a.total; g += ncl, ++it) {
         const int buf = it & 1;
         const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
@@ -1300,20 +1313,13 @@ __device__ __forceinline__ void run_mma_pair(const KernelArgs &a, uint32_t tmem,
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = ptx::smem_u32(smem + stage * Cfg::kStageBytes);
-            const uint32_t sb = sa + Cfg::kABytes;
+            const uint32_t so = stage * Cfg::kStageBytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                // Same descriptors as the single-CTA kernel: they describe this
-                // CTA's 128 rows of A and BN/2 columns of B.  The peer CTA holds
-                // its halves at the same offsets.
-                const uint64_t ad = ptx::sdesc_sw128(sa + kk * 32, 0, 1024);
-                const uint64_t bd = ptx::sdesc_sw128(sb + kk * 2048, 8192, 1024);
-                ptx::mma_bf16_ss_pair(d, ad, bd, Cfg::kIdesc, (kb | kk) != 0 ? 1u : 0u);
-            }
-            const uint32_t eb = ptx::smem_u32(&ctl->empty[stage]);
-            ptx::mma_commit_pair(ptx::mapa(eb, 0));
-            ptx::mma_commit_pair(ptx::mapa(eb, 1));
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                ptx::mma_bf16_ss_pair(d, ptx::sdesc_advance(ad0, so + kk * 32),
+                                      ptx::sdesc_advance(bd0, so + kk * 2048), Cfg::kIdesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+            ptx::mma_commit_pair_both(empty0 + stage * 8u);
             if (++stage == Cfg::kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -1323,8 +1329,7 @@ __device__ __forceinline__ void run_mma_pair(const KernelArgs &a, uint32_t tmem,
             break;
         const uint32_t ab = ptx::smem_u32(&ctl->acc_full[buf]);
         if (a.nK > 0) {
-            ptx::mma_commit_pair(ptx::mapa(ab, 0));
-            ptx::mma_commit_pair(ptx::mapa(ab, 1));
+            ptx::mma_commit_pair_both(ab);
         } else {
             ptx::mbar_arrive_cluster(ptx::mapa(ab, 0));
             ptx::mbar_arrive_cluster(ptx::mapa(ab, 1));

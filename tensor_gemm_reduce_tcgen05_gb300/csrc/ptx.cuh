@@ -227,6 +227,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The descriptor of the same layout `bytes` further on in shared memory: the
+// start address field holds address / 16 in 14 bits, and a shared-memory
+// address stays below 2^18, so the addition never carries into the next
+// field.  Cheaper than rebuilding the descriptor, on the MMA thread's path.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes)
+{
+    return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and an fp32
 // accumulator.
 //   bits  4-5   D format (1 = f32)
@@ -373,6 +382,16 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t cluster_addr)
 {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      cluster_addr)
+                 : "memory");
+}
+
+// Arrive once on the mbarrier at shared-memory offset `bar` in both CTAs of the
+// pair (cluster ranks 0 and 1) when every pair MMA this thread issued so far
+// has completed: one commit in place of one per CTA.
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"(static_cast<uint16_t>(3))
                  : "memory");
 }
 
