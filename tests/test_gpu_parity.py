@@ -108,12 +108,20 @@ def test_beta_zero_ignores_nan_c():
     np.testing.assert_array_equal(to_np_y(Y), oracle_y(A, B, None, 1.0, 0.0, "fp32"))
 
 
-def test_k_zero_gives_w_beta_c():
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("tile_m", [None, 256])
+def test_k_zero_gives_w_beta_c(tile_m, mode):
+    """K = 0: no MMA runs, so the MMA thread hands each accumulator over by a
+    plain arrival (on both CTAs' barriers in the CTA-pair kernel, tile_m = 256)
+    and the epilogue reads zeros instead of TMEM; Y = W * beta * C exactly."""
     W, M, N = 4, 256, 264
     _, _, C = inputs(W, M, N, 8, "int", c_dist="normal1")
     A = torch.zeros((W, M, 0), dtype=torch.bfloat16)
     B = torch.zeros((W, 0, N), dtype=torch.bfloat16)
-    y, _, _ = run_gpu(A, B, C, W, M, N, 0, 1.0, 1.0, "fp32")
+    y, plan, _ = run_gpu(A, B, C, W, M, N, 0, 1.0, 1.0, "fp32", tile_m=tile_m, reduce_mode=mode,
+                         poison=True, calls=2)
+    if tile_m is not None:
+        assert plan["bm"] == tile_m
     np.testing.assert_array_equal(y, W * C.float().numpy())
 
 
